@@ -1,0 +1,155 @@
+/*
+ * moe.h — C ABI of libmoe: the local Mixture-of-Experts forward on one GB300 (sm_103a).
+ *
+ * The operation is the MoE sequence of the ruDNN user guide (docs.rs, ruDNN 0.1.72,
+ * docs/de/README.md), §3 "MoE-Workflow": router logits -> softmax / top-k -> compact dispatch ->
+ * bias-free SwiGLU experts -> weighted combine that restores token order.  Each entry point below
+ * is one stage of §6 "MoE aufrufen" (route, RoutingPlan::dispatch, forward_dispatched, combine)
+ * or the whole forward.
+ *
+ * Conventions shared by every entry point
+ *  - Buffers are DEVICE pointers owned by the caller, contiguous and row-major.  The library never
+ *    allocates, frees or synchronises on these paths; scratch memory comes from the caller through
+ *    (ws, ws_bytes), sized by the matching *_workspace_bytes() query.
+ *  - Work is enqueued on the caller's stream `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  Every call returns as soon as the work is enqueued.
+ *  - Every argument is checked on the host before anything is enqueued; a rejected call enqueues
+ *    nothing and returns the status below.  T = 0 is valid and enqueues nothing.
+ *  - MOE_ERR_CUDA means a CUDA launch or query failed (including "no device").
+ *  - Kernels never trap.  Conditions only the device can see (an expert index >= E handed to
+ *    moe_dispatch; a pipeline wait in the tensor-core kernels that exceeded its time limit) are
+ *    recorded in a status word at the start of the workspace; moe_device_status() reads it.
+ *  - dtype codes: MOE_F32, MOE_F16, MOE_BF16 (unquantised, as §4 "Routing-Vertrag" requires).
+ *  - Limits: 1 <= top_k <= E <= 1024; T * top_k < 2^31; H, I >= 1.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = 1,      /* a required pointer is NULL                                  */
+  MOE_ERR_SHAPE = 2,     /* sizes out of range or inconsistent (incl. top_k > E)        */
+  MOE_ERR_DTYPE = 3,     /* dtype code unknown or not allowed for this argument          */
+  MOE_ERR_ALIGN = 4,     /* pointer or row pitch breaks the 16-byte rule of the kernels   */
+  MOE_ERR_WORKSPACE = 5, /* ws is NULL, misaligned or smaller than the query result       */
+  MOE_ERR_CUDA = 6,      /* CUDA runtime / launch error                                   */
+  MOE_ERR_TIMEOUT = 7,   /* (device status only) a pipeline wait exceeded its time limit  */
+  MOE_ERR_INDEX = 8      /* (device status only) an expert index >= E reached dispatch    */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_F16 = 1, MOE_BF16 = 2 } moe_dtype;
+
+/* Static text for a status code (never NULL). */
+const char* moe_status_string(int status);
+
+/* ABI version of this header (bumped on any signature change). */
+int moe_abi_version(void);
+
+/*
+ * moe_route — route(logits, RoutingOptions{top_k, renormalize}) of §3/§4 "Routing-Vertrag".
+ *
+ * logits  [T, E] in dtype `ldt` (f32 / f16 / bf16).
+ * idx     [T, top_k] uint32 out: selected experts, ordered by descending weight; equal logits
+ *         give the lower expert id first.  Selection ranks experts by their logit (the ranking
+ *         of the exact softmax).
+ * w       [T, top_k] out, dtype `ldt`: p_e = exp(l_e - max) / sum_all exp(l - max) computed in
+ *         FP32 over all E experts; with renormalize != 0 the selected p are divided by their sum;
+ *         then cast (round-to-nearest-even) to `ldt`.
+ * Rows holding a NaN, a +inf, or only -inf get NaN weights and indices 0..top_k-1 (they are
+ * still dispatched; nothing is dropped).
+ * Alignment: none required (16-byte aligned rows take a vectorised path).
+ */
+int moe_route(const void* logits, int ldt, int64_t T, int64_t E, int top_k, int renormalize,
+              uint32_t* idx, void* w, moe_stream_t stream);
+
+/*
+ * moe_dispatch — RoutingPlan::dispatch(input) of §3/§5 "Expertengewichte und Verteilung".
+ *
+ * Capacity-free: every one of the R = T*top_k routed slots (slot s = t*top_k + j) becomes one
+ * dispatched row.  Rows are grouped by expert; inside an expert they keep ascending slot order,
+ * so the result does not depend on thread timing.
+ *
+ * x            [T, H] tokens, dtype `xdt`.
+ * idx          [T, top_k] uint32 expert ids (from moe_route or the caller; ids >= E are not
+ *              dispatched, their row_of_slot entry is 0xFFFFFFFF and the device status records
+ *              MOE_ERR_INDEX).
+ * x_d          [R, H] out, dtype `xdt`: x_d[r] = x[token_of_row[r]].
+ * offsets      [E + 1] int32 out: rows of expert e are offsets[e] .. offsets[e+1]-1.
+ * token_of_row [R] uint32 out: token feeding row r.
+ * row_of_slot  [R] uint32 out: row holding slot s (the saved map that restores token order).
+ * ws           workspace of at least moe_dispatch_workspace_bytes(T, E, top_k) bytes,
+ *              16-byte aligned; contents on entry are ignored.
+ * Alignment: x and x_d 16-byte aligned with H * sizeof(xdt) a multiple of 16, else MOE_ERR_ALIGN.
+ */
+size_t moe_dispatch_workspace_bytes(int64_t T, int64_t E, int top_k);
+int moe_dispatch(const void* x, int xdt, int64_t T, int64_t H, const uint32_t* idx, int64_t E,
+                 int top_k, void* x_d, int32_t* offsets, uint32_t* token_of_row,
+                 uint32_t* row_of_slot, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_experts_forward_dispatched — SwiGluExperts::forward_dispatched of §3/§5/§6.
+ *
+ * For every expert e and every row r in offsets[e] .. offsets[e+1]-1:
+ *   g = x_d[r] gate[e]^T,  u = x_d[r] up[e]^T          (both [I])
+ *   a = silu(g) * u,       silu(z) = z / (1 + exp(-z))
+ *   y[r] = a down[e]^T                                  ([H]); no bias.
+ * x_d [rows, H], gate/up [E, I, H], down [E, H, I], y [rows, H]; all in dtype `wdt`.
+ * offsets [E + 1] int32 on the device (non-decreasing, offsets[0] = 0, offsets[E] <= rows).
+ * bf16 / f16: 5th-generation tensor cores, FP32 accumulation, `a` rounded to `wdt` between the
+ *   two projections, y rounded once.  Requires H % 8 == 0, I % 8 == 0 and 16-byte aligned
+ *   pointers (TMA), else MOE_ERR_ALIGN.
+ * f32: FP32 CUDA-core GEMMs, `a` kept in FP32.
+ * ws: at least moe_experts_workspace_bytes(rows, E, H, I, wdt) bytes, 256-byte aligned.
+ */
+size_t moe_experts_workspace_bytes(int64_t rows, int64_t E, int64_t H, int64_t I, int wdt);
+int moe_experts_forward_dispatched(const void* x_d, const int32_t* offsets, int64_t rows,
+                                   const void* gate, const void* up, const void* down, int wdt,
+                                   int64_t E, int64_t H, int64_t I, void* y, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_combine — DispatchedTokens::combine(expert_output) of §3/§6.
+ *
+ * out[t] = sum_{j = 0..top_k-1} w[t, j] * y[row_of_slot[t*top_k + j]], accumulated in FP32 in
+ * that fixed slot order (run-to-run deterministic), rounded once to `ydt`.  A slot whose
+ * row_of_slot is 0xFFFFFFFF (an undispatched invalid index) makes the token's row NaN.
+ * y [R, H] dtype `ydt`; w [T, top_k] dtype `wdt` (the logits dtype); out [T, H] dtype `ydt`.
+ * Alignment: none required (16-byte aligned rows take a vectorised path).
+ */
+int moe_combine(const void* y, int ydt, const uint32_t* row_of_slot, const void* w, int wdt,
+                int64_t T, int64_t H, int top_k, void* out, moe_stream_t stream);
+
+/*
+ * moe_forward — SwiGluExperts::forward(input, logits, options) of §6: route, dispatch, experts
+ * and combine on one stream with no host synchronisation.
+ * x [T, H] and the expert weights share dtype `wdt`; logits [T, E] have dtype `ldt`;
+ * out [T, H] has dtype `wdt`.  Same alignment rules as the stages.
+ * ws: at least moe_forward_workspace_bytes(T, E, H, I, top_k, ldt, wdt) bytes, 256-byte aligned.
+ */
+size_t moe_forward_workspace_bytes(int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
+                                   int ldt, int wdt);
+int moe_forward(const void* x, const void* logits, int ldt, const void* gate, const void* up,
+                const void* down, int wdt, int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
+                int renormalize, void* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_device_status — synchronises `stream`, then reads and clears the status word at the start
+ * of a workspace used by moe_dispatch, moe_experts_forward_dispatched or moe_forward.
+ * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_INDEX, or MOE_ERR_CUDA if the read itself failed.
+ */
+int moe_device_status(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

@@ -1,5 +1,8 @@
 """GB300 (sm_103a) local MoE forward: route -> dispatch -> SwiGLU experts -> combine.
 
-The compute lives in ``libmoe.so`` (hand-written CUDA kernels behind a C ABI declared in
+The compute lives in ``libmoe.so`` (hand-written CUDA kernels behind the C ABI declared in
 ``include/moe.h``); ``binding`` marshals torch tensors into that ABI and nothing else.
 """
+from .binding import (MoeError, dispatch_workspace_bytes, experts_workspace_bytes,  # noqa: F401
+                      forward_workspace_bytes, moe_combine, moe_device_status, moe_dispatch,
+                      moe_experts_forward_dispatched, moe_forward, moe_route)

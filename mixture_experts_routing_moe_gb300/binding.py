@@ -1,0 +1,202 @@
+"""ctypes binding of libmoe (include/moe.h).  Argument marshalling only.
+
+Every function here takes torch CUDA tensors, checks that they are contiguous CUDA tensors,
+allocates missing outputs / workspace with torch (device memory is the one thing torch is used
+for), and passes raw pointers, sizes and the current stream to the C ABI.  All computation runs
+in libmoe's kernels; there is no CPU path.  A missing or unbuilt library raises at first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "moe.h")
+
+MOE_F32, MOE_F16, MOE_BF16 = 0, 1, 2
+DTYPE_CODE = {torch.float32: MOE_F32, torch.float16: MOE_F16, torch.bfloat16: MOE_BF16}
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_NULL", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR_DTYPE",
+          4: "MOE_ERR_ALIGN", 5: "MOE_ERR_WORKSPACE", 6: "MOE_ERR_CUDA", 7: "MOE_ERR_TIMEOUT",
+          8: "MOE_ERR_INDEX"}
+
+_i64, _int, _sz, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+_SIGS = {
+    "moe_abi_version": (_int, []),
+    "moe_status_string": (ctypes.c_char_p, [_int]),
+    "moe_route": (_int, [_vp, _int, _i64, _i64, _int, _int, _vp, _vp, _vp]),
+    "moe_dispatch_workspace_bytes": (_sz, [_i64, _i64, _int]),
+    "moe_dispatch": (_int, [_vp, _int, _i64, _i64, _vp, _i64, _int, _vp, _vp, _vp, _vp, _vp, _sz,
+                            _vp]),
+    "moe_experts_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _int]),
+    "moe_experts_forward_dispatched": (_int, [_vp, _vp, _i64, _vp, _vp, _vp, _int, _i64, _i64,
+                                              _i64, _vp, _vp, _sz, _vp]),
+    "moe_combine": (_int, [_vp, _int, _vp, _vp, _int, _i64, _i64, _int, _vp, _vp]),
+    "moe_forward_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _int, _int, _int]),
+    "moe_forward": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _int, _i64, _i64, _i64, _i64, _int, _int,
+                           _vp, _vp, _sz, _vp]),
+    "moe_device_status": (_int, [_vp, _sz, _vp]),
+}
+
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} "
+                         f"({lib().moe_status_string(status).decode()})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libmoe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m mixture_experts_routing_moe_gb300.build` (needs nvcc)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype, f.argtypes = res, args
+        _lib = L
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/moe.h declares."""
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise MoeError(st, where)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("libmoe takes contiguous CUDA tensors")
+
+
+def _code(t) -> int:
+    try:
+        return DTYPE_CODE[t.dtype]
+    except KeyError:
+        raise MoeError(3, f"dtype {t.dtype}") from None
+
+
+# ------------------------------------------------------------------------------ entry points
+def moe_route(logits, top_k: int, renormalize: bool = True, idx=None, w=None, stream=None):
+    """route(logits, RoutingOptions{top_k, renormalize}) -> (idx uint32 [T,k], w [T,k])."""
+    _cuda(logits)
+    T, E = logits.shape
+    if idx is None:
+        idx = torch.empty(T, top_k, dtype=torch.uint32, device=logits.device)
+    if w is None:
+        w = torch.empty(T, top_k, dtype=logits.dtype, device=logits.device)
+    _cuda(idx, w)
+    _check(lib().moe_route(_ptr(logits), _code(logits), T, E, top_k, int(bool(renormalize)),
+                           _ptr(idx), _ptr(w), _stream(stream)), "moe_route")
+    return idx, w
+
+
+def dispatch_workspace_bytes(T: int, E: int, top_k: int) -> int:
+    return lib().moe_dispatch_workspace_bytes(T, E, top_k)
+
+
+def moe_dispatch(x, idx, E: int, x_d=None, offsets=None, token_of_row=None, row_of_slot=None,
+                 ws=None, stream=None):
+    """RoutingPlan::dispatch -> dict(x_d, offsets, token_of_row, row_of_slot, ws)."""
+    _cuda(x, idx)
+    T, H = x.shape
+    k = idx.shape[1]
+    R, dev = T * k, x.device
+    x_d = torch.empty(R, H, dtype=x.dtype, device=dev) if x_d is None else x_d
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
+    token_of_row = (torch.empty(R, dtype=torch.uint32, device=dev) if token_of_row is None
+                    else token_of_row)
+    row_of_slot = (torch.empty(R, dtype=torch.uint32, device=dev) if row_of_slot is None
+                   else row_of_slot)
+    if ws is None:
+        ws = torch.empty(max(dispatch_workspace_bytes(T, E, k), 256), dtype=torch.uint8,
+                         device=dev)
+    _cuda(x_d, offsets, token_of_row, row_of_slot, ws)
+    _check(lib().moe_dispatch(_ptr(x), _code(x), T, H, _ptr(idx), E, k, _ptr(x_d), _ptr(offsets),
+                              _ptr(token_of_row), _ptr(row_of_slot), _ptr(ws), ws.numel(),
+                              _stream(stream)), "moe_dispatch")
+    return {"x_d": x_d, "offsets": offsets, "token_of_row": token_of_row,
+            "row_of_slot": row_of_slot, "ws": ws}
+
+
+def experts_workspace_bytes(rows: int, E: int, H: int, I: int, dtype) -> int:
+    return lib().moe_experts_workspace_bytes(rows, E, H, I, DTYPE_CODE[dtype])
+
+
+def moe_experts_forward_dispatched(x_d, offsets, gate, up, down, y=None, ws=None, stream=None):
+    """SwiGluExperts::forward_dispatched -> y [rows, H]."""
+    _cuda(x_d, offsets, gate, up, down)
+    rows, H = x_d.shape
+    E, I, _ = gate.shape
+    y = torch.empty(rows, H, dtype=x_d.dtype, device=x_d.device) if y is None else y
+    if ws is None:
+        ws = torch.empty(max(experts_workspace_bytes(rows, E, H, I, gate.dtype), 256),
+                         dtype=torch.uint8, device=x_d.device)
+    _cuda(y, ws)
+    _check(lib().moe_experts_forward_dispatched(
+        _ptr(x_d), _ptr(offsets), rows, _ptr(gate), _ptr(up), _ptr(down), _code(gate), E, H, I,
+        _ptr(y), _ptr(ws), ws.numel(), _stream(stream)), "moe_experts_forward_dispatched")
+    return y
+
+
+def moe_combine(y, row_of_slot, w, out=None, stream=None):
+    """DispatchedTokens::combine -> out [T, H] in y's dtype."""
+    _cuda(y, row_of_slot, w)
+    T, k = w.shape
+    H = y.shape[1]
+    out = torch.empty(T, H, dtype=y.dtype, device=y.device) if out is None else out
+    _cuda(out)
+    _check(lib().moe_combine(_ptr(y), _code(y), _ptr(row_of_slot), _ptr(w), _code(w), T, H, k,
+                             _ptr(out), _stream(stream)), "moe_combine")
+    return out
+
+
+def forward_workspace_bytes(T, E, H, I, top_k, logits_dtype, dtype) -> int:
+    return lib().moe_forward_workspace_bytes(T, E, H, I, top_k, DTYPE_CODE[logits_dtype],
+                                             DTYPE_CODE[dtype])
+
+
+def moe_forward(x, logits, gate, up, down, top_k: int, renormalize: bool = True, out=None,
+                ws=None, stream=None):
+    """SwiGluExperts::forward(input, logits, options) -> out [T, H]."""
+    _cuda(x, logits, gate, up, down)
+    T, H = x.shape
+    E, I, _ = gate.shape
+    out = torch.empty_like(x) if out is None else out
+    if ws is None:
+        ws = torch.empty(max(forward_workspace_bytes(T, E, H, I, top_k, logits.dtype, x.dtype), 256),
+                         dtype=torch.uint8, device=x.device)
+    _cuda(out, ws)
+    _check(lib().moe_forward(_ptr(x), _ptr(logits), _code(logits), _ptr(gate), _ptr(up),
+                             _ptr(down), _code(gate), T, E, H, I, top_k, int(bool(renormalize)),
+                             _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "moe_forward")
+    return out
+
+
+def moe_device_status(ws, stream=None) -> int:
+    """Synchronise, read and clear the workspace status word (0 = MOE_OK)."""
+    return lib().moe_device_status(_ptr(ws), ws.numel(), _stream(stream))

@@ -1,0 +1,243 @@
+// C-ABI entry points of libmoe (declared in include/moe.h): host-side validation, workspace
+// layout and the launch sequence.  No entry point allocates, frees or synchronises, except
+// moe_device_status, whose job is to read the device status word back.
+#include <string.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kMaxE = 1024;
+constexpr int64_t kMaxRows = (int64_t)1 << 31;
+
+size_t dtype_size(int dt) { return dt == MOE_F32 ? 4 : (dt == MOE_F16 || dt == MOE_BF16) ? 2 : 0; }
+bool valid_dtype(int dt) { return dtype_size(dt) != 0; }
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+struct Cursor {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  }
+};
+
+struct FwdLayout {
+  size_t idx, w, ros, tor, offsets, hist, xd, a, total;
+};
+FwdLayout fwd_layout(int64_t T, int64_t E, int64_t H, int64_t I, int k, int ldt, int wdt) {
+  const int64_t R = T * k;
+  FwdLayout l;
+  Cursor c;
+  c.take(kWsHeader);
+  l.idx = c.take((size_t)R * 4);
+  l.w = c.take((size_t)R * dtype_size(ldt));
+  l.ros = c.take((size_t)R * 4);
+  l.tor = c.take((size_t)R * 4);
+  l.offsets = c.take((size_t)(E + 1) * 4);
+  l.hist = c.take(dispatch_scratch_bytes(R, (int)E));
+  l.xd = c.take((size_t)R * H * dtype_size(wdt));  // x_d, later reused for y
+  l.a = c.take((size_t)R * I * dtype_size(wdt));
+  l.total = c.off;
+  return l;
+}
+
+int check_route_shape(int64_t T, int64_t E, int top_k) {
+  if (T < 0 || E < 1 || E > kMaxE || top_k < 1 || top_k > E) return MOE_ERR_SHAPE;
+  if (T * top_k >= kMaxRows) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+// Conditions of the tensor-core path: 16-byte aligned operands and 16-byte row pitches for TMA.
+int check_tc_align(int64_t H, int64_t I, const void* const* ptrs, int n) {
+  if (H % 8 != 0 || I % 8 != 0) return MOE_ERR_ALIGN;
+  for (int i = 0; i < n; ++i)
+    if (!aligned16(ptrs[i])) return MOE_ERR_ALIGN;
+  return MOE_OK;
+}
+
+int check_experts_shape(int64_t rows, int64_t E, int64_t H, int64_t I) {
+  if (rows < 0 || rows >= kMaxRows || E < 1 || E > kMaxE || H < 1 || I < 1) return MOE_ERR_SHAPE;
+  if (E * I >= kMaxRows || E * H >= kMaxRows) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+int run_experts(const void* x_d, const int32_t* offsets, int64_t rows, const void* gate,
+                const void* up, const void* down, int wdt, int64_t E, int64_t H, int64_t I,
+                void* y, void* a, unsigned* status, cudaStream_t s) {
+  if (wdt == MOE_F32)
+    return cuda_status(launch_experts_simt((const float*)x_d, offsets, rows, (const float*)gate,
+                                           (const float*)up, (const float*)down, (int)E, (int)H,
+                                           (int)I, (float*)y, (float*)a, s));
+  return cuda_status(launch_experts_tc(x_d, offsets, rows, gate, up, down, wdt, (int)E, (int)H,
+                                       (int)I, y, a, status, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return 1; }
+
+const char* moe_status_string(int st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "a required pointer is NULL";
+    case MOE_ERR_SHAPE: return "sizes out of range or inconsistent";
+    case MOE_ERR_DTYPE: return "dtype not allowed for this argument";
+    case MOE_ERR_ALIGN: return "pointer or row pitch not 16-byte aligned";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "a device pipeline wait timed out";
+    case MOE_ERR_INDEX: return "an expert index >= E reached dispatch";
+  }
+  return "unknown status";
+}
+
+int moe_route(const void* logits, int ldt, int64_t T, int64_t E, int top_k, int renormalize,
+              uint32_t* idx, void* w, moe_stream_t stream) {
+  if (!valid_dtype(ldt)) return MOE_ERR_DTYPE;
+  int st = check_route_shape(T, E, top_k);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!logits || !idx || !w) return MOE_ERR_NULL;
+  return cuda_status(launch_route(logits, ldt, T, (int)E, top_k, renormalize != 0, idx, w,
+                                  (cudaStream_t)stream));
+}
+
+size_t moe_dispatch_workspace_bytes(int64_t T, int64_t E, int top_k) {
+  if (check_route_shape(T, E, top_k) != MOE_OK) return 0;
+  return align_up(kWsHeader, 256) + dispatch_scratch_bytes(T * top_k, (int)E);
+}
+
+int moe_dispatch(const void* x, int xdt, int64_t T, int64_t H, const uint32_t* idx, int64_t E,
+                 int top_k, void* x_d, int32_t* offsets, uint32_t* token_of_row,
+                 uint32_t* row_of_slot, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!valid_dtype(xdt)) return MOE_ERR_DTYPE;
+  int st = check_route_shape(T, E, top_k);
+  if (st != MOE_OK) return st;
+  if (H < 1) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!x || !idx || !x_d || !offsets || !token_of_row || !row_of_slot) return MOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(x_d) || (H * (int64_t)dtype_size(xdt)) % 16 != 0)
+    return MOE_ERR_ALIGN;
+  if (!ws || !aligned16(ws) || ws_bytes < moe_dispatch_workspace_bytes(T, E, top_k))
+    return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned* status = (unsigned*)ws;
+  cudaError_t err = cudaMemsetAsync(status, 0, sizeof(unsigned), s);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t* hist = (int32_t*)((uint8_t*)ws + align_up(kWsHeader, 256));
+  return cuda_status(launch_dispatch(x, xdt, T, H, idx, (int)E, top_k, x_d, offsets,
+                                     token_of_row, row_of_slot, hist, status, s));
+}
+
+size_t moe_experts_workspace_bytes(int64_t rows, int64_t E, int64_t H, int64_t I, int wdt) {
+  if (!valid_dtype(wdt) || check_experts_shape(rows, E, H, I) != MOE_OK) return 0;
+  return align_up(kWsHeader, 256) + align_up((size_t)rows * I * dtype_size(wdt), 256);
+}
+
+int moe_experts_forward_dispatched(const void* x_d, const int32_t* offsets, int64_t rows,
+                                   const void* gate, const void* up, const void* down, int wdt,
+                                   int64_t E, int64_t H, int64_t I, void* y, void* ws,
+                                   size_t ws_bytes, moe_stream_t stream) {
+  if (!valid_dtype(wdt)) return MOE_ERR_DTYPE;
+  int st = check_experts_shape(rows, E, H, I);
+  if (st != MOE_OK) return st;
+  if (!gate || !up || !down) return MOE_ERR_NULL;
+  if (rows == 0) return MOE_OK;
+  if (!x_d || !offsets || !y) return MOE_ERR_NULL;
+  if (!ws || ((uintptr_t)ws & 255u) != 0 ||
+      ws_bytes < moe_experts_workspace_bytes(rows, E, H, I, wdt))
+    return MOE_ERR_WORKSPACE;
+  void* a = (uint8_t*)ws + align_up(kWsHeader, 256);
+  if (wdt != MOE_F32) {
+    const void* ptrs[5] = {x_d, gate, up, down, y};
+    st = check_tc_align(H, I, ptrs, 5);
+    if (st != MOE_OK) return st;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned* status = (unsigned*)ws;
+  if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return MOE_ERR_CUDA;
+  return run_experts(x_d, offsets, rows, gate, up, down, wdt, E, H, I, y, a, status, s);
+}
+
+int moe_combine(const void* y, int ydt, const uint32_t* row_of_slot, const void* w, int wdt,
+                int64_t T, int64_t H, int top_k, void* out, moe_stream_t stream) {
+  if (!valid_dtype(ydt) || !valid_dtype(wdt)) return MOE_ERR_DTYPE;
+  if (T < 0 || H < 1 || top_k < 1 || top_k > kMaxE || T * top_k >= kMaxRows) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!y || !row_of_slot || !w || !out) return MOE_ERR_NULL;
+  return cuda_status(launch_combine(y, ydt, row_of_slot, w, wdt, T, H, top_k, out,
+                                    (cudaStream_t)stream));
+}
+
+size_t moe_forward_workspace_bytes(int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
+                                   int ldt, int wdt) {
+  if (!valid_dtype(ldt) || !valid_dtype(wdt)) return 0;
+  if (check_route_shape(T, E, top_k) != MOE_OK || check_experts_shape(T * top_k, E, H, I) != MOE_OK)
+    return 0;
+  return fwd_layout(T, E, H, I, top_k, ldt, wdt).total;
+}
+
+int moe_forward(const void* x, const void* logits, int ldt, const void* gate, const void* up,
+                const void* down, int wdt, int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
+                int renormalize, void* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!valid_dtype(ldt) || !valid_dtype(wdt)) return MOE_ERR_DTYPE;
+  int st = check_route_shape(T, E, top_k);
+  if (st != MOE_OK) return st;
+  st = check_experts_shape(T * top_k, E, H, I);
+  if (st != MOE_OK) return st;
+  if (!gate || !up || !down) return MOE_ERR_NULL;
+  if (T == 0) return MOE_OK;
+  if (!x || !logits || !out) return MOE_ERR_NULL;
+  if (!aligned16(x) || (H * (int64_t)dtype_size(wdt)) % 16 != 0) return MOE_ERR_ALIGN;
+  if (wdt != MOE_F32) {
+    const void* ptrs[5] = {x, gate, up, down, out};
+    st = check_tc_align(H, I, ptrs, 5);
+    if (st != MOE_OK) return st;
+  }
+  const FwdLayout L = fwd_layout(T, E, H, I, top_k, ldt, wdt);
+  if (!ws || ((uintptr_t)ws & 255u) != 0 || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* b = (uint8_t*)ws;
+  unsigned* status = (unsigned*)ws;
+  uint32_t* idx = (uint32_t*)(b + L.idx);
+  void* w = b + L.w;
+  uint32_t* ros = (uint32_t*)(b + L.ros);
+  uint32_t* tor = (uint32_t*)(b + L.tor);
+  int32_t* offsets = (int32_t*)(b + L.offsets);
+  int32_t* hist = (int32_t*)(b + L.hist);
+  void* xd = b + L.xd;
+  void* a = b + L.a;
+  const int64_t R = T * top_k;
+
+  if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t err = launch_route(logits, ldt, T, (int)E, top_k, renormalize != 0, idx, w, s);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  err = launch_dispatch(x, wdt, T, H, idx, (int)E, top_k, xd, offsets, tor, ros, hist, status, s);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  st = run_experts(xd, offsets, R, gate, up, down, wdt, E, H, I, /*y=*/xd, a, status, s);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_combine(xd, wdt, ros, w, ldt, T, H, top_k, out, s));
+}
+
+int moe_device_status(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws || ws_bytes < sizeof(unsigned)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&v, ws, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(ws, 0, sizeof(unsigned)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v & kStatusTimeout) return MOE_ERR_TIMEOUT;
+  if (v & kStatusIndex) return MOE_ERR_INDEX;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,115 @@
+// Combine: DispatchedTokens::combine of the ruDNN user guide, §3 "MoE-Workflow" / §6 "MoE aufrufen".
+//
+// out[t] = sum_{j=0..k-1} w[t, j] * y[row_of_slot[t*k + j]], FP32 accumulation in the fixed slot
+// order j = 0..k-1 (no atomics: the result is the same bits on every run), rounded once to the
+// output dtype.  One warp per token; lane i handles 16-byte column chunks i, i+32, ...  The k
+// (row, weight) pairs of a token are loaded by the lanes once and broadcast with shuffles.
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int kCombWarps = 8;
+
+template <typename TY, typename TW, bool VEC>
+__global__ void __launch_bounds__(kCombWarps * 32)
+    moe_combine_kernel(const TY* __restrict__ y, const uint32_t* __restrict__ row_of_slot,
+                       const TW* __restrict__ w, int64_t T, int64_t H, int k,
+                       TY* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * kCombWarps + (threadIdx.x >> 5);
+  if (t >= T) return;
+  constexpr int VW = VEC ? 16 / (int)sizeof(TY) : 1;
+  const int64_t chunks = H / VW;
+  for (int64_t c0 = 0; c0 < chunks; c0 += 32) {
+    const int64_t c = c0 + lane;
+    float acc[VW];
+#pragma unroll
+    for (int i = 0; i < VW; ++i) acc[i] = 0.f;
+    bool poisoned = false;
+    for (int jb = 0; jb < k; jb += 32) {
+      uint32_t my_row = kInvalidRow;
+      float my_w = 0.f;
+      if (jb + lane < k) {
+        my_row = row_of_slot[t * k + jb + lane];
+        my_w = Dt<TW>::to_f(w[t * k + jb + lane]);
+      }
+      const int nj = min(32, k - jb);
+      for (int jj = 0; jj < nj; ++jj) {
+        const uint32_t r = __shfl_sync(0xFFFFFFFFu, my_row, jj);
+        const float wj = __shfl_sync(0xFFFFFFFFu, my_w, jj);
+        if (r == kInvalidRow) {
+          poisoned = true;
+          continue;
+        }
+        if (c < chunks) {
+          if (VEC) {
+            Vec16<TY> q;
+            q.u = ld_nc_v4(y + (int64_t)r * H + c * VW);
+            float f[VW];
+            q.to_float(f);
+#pragma unroll
+            for (int i = 0; i < VW; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+          } else {
+            acc[0] = fmaf(wj, Dt<TY>::to_f(y[(int64_t)r * H + c]), acc[0]);
+          }
+        }
+      }
+    }
+    if (c < chunks) {
+      if (poisoned) {
+#pragma unroll
+        for (int i = 0; i < VW; ++i) acc[i] = __int_as_float(0x7FC00000);
+      }
+      if (VEC) {
+        Vec16<TY> q;
+        q.from_float(acc);
+        st_v4(out + t * H + c * VW, q.u);
+      } else {
+        out[t * H + c] = Dt<TY>::from_f(acc[0]);
+      }
+    }
+  }
+}
+
+template <typename TY, typename TW>
+cudaError_t launch_combine_t(const void* y, const uint32_t* ros, const void* w, int64_t T,
+                             int64_t H, int k, void* out, cudaStream_t s) {
+  const bool vec = ((uintptr_t)y % 16 == 0) && ((uintptr_t)out % 16 == 0) &&
+                   ((H * (int64_t)sizeof(TY)) % 16 == 0);
+  const unsigned blocks = (unsigned)((T + kCombWarps - 1) / kCombWarps);
+  if (vec)
+    moe_combine_kernel<TY, TW, true><<<blocks, kCombWarps * 32, 0, s>>>(
+        (const TY*)y, ros, (const TW*)w, T, H, k, (TY*)out);
+  else
+    moe_combine_kernel<TY, TW, false><<<blocks, kCombWarps * 32, 0, s>>>(
+        (const TY*)y, ros, (const TW*)w, T, H, k, (TY*)out);
+  return cudaGetLastError();
+}
+
+template <typename TY>
+cudaError_t launch_combine_y(const void* y, const uint32_t* ros, const void* w, int wdt,
+                             int64_t T, int64_t H, int k, void* out, cudaStream_t s) {
+  switch (wdt) {
+    case MOE_F32: return launch_combine_t<TY, float>(y, ros, w, T, H, k, out, s);
+    case MOE_F16: return launch_combine_t<TY, __half>(y, ros, w, T, H, k, out, s);
+    case MOE_BF16: return launch_combine_t<TY, __nv_bfloat16>(y, ros, w, T, H, k, out, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const void* y, int ydt, const uint32_t* row_of_slot, const void* w,
+                           int wdt, int64_t T, int64_t H, int k, void* out, cudaStream_t s) {
+  switch (ydt) {
+    case MOE_F32: return launch_combine_y<float>(y, row_of_slot, w, wdt, T, H, k, out, s);
+    case MOE_F16: return launch_combine_y<__half>(y, row_of_slot, w, wdt, T, H, k, out, s);
+    case MOE_BF16:
+      return launch_combine_y<__nv_bfloat16>(y, row_of_slot, w, wdt, T, H, k, out, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -1,0 +1,195 @@
+// Dispatch: RoutingPlan::dispatch of the ruDNN user guide, §5 "Expertengewichte und Verteilung".
+//
+// Capacity-free and deterministic.  The page leaves the order inside an expert open (it comes
+// from atomics there); here rows keep ascending slot order s = t*k + j, built as a stable
+// counting sort without atomics on global memory:
+//   1. count   — warp w owns slots [w*CH, w*CH + CH); it histograms its chunk in a warp-private
+//                shared-memory array (lanes with the same expert are merged with match.any) and
+//                writes hist[w][e].
+//   2. scan    — one block: hist[w][e] becomes the exclusive prefix over w (per expert), and
+//                offsets = exclusive prefix over e of the per-expert totals.
+//   3. scatter — warp w walks its chunk again in slot order; a slot's row is
+//                offsets[e] + hist[w][e] + (earlier slots of the chunk with the same expert), the
+//                last term from match.any ranks.  Writes row_of_slot and token_of_row.
+//   4. rows    — one block per token reads x[t] once (16-byte loads) and writes it to the k rows
+//                row_of_slot[t*k + 0..k-1] of x_d.
+// Expert ids >= E are not dispatched: their row_of_slot is 0xFFFFFFFF and the status word gets
+// the index bit.  No access goes out of bounds for any id value.
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int kDispWarps = 4;  // warps per block in count / scatter
+constexpr int kMaxE = 1024;
+
+__global__ void __launch_bounds__(kDispWarps * 32)
+    moe_dispatch_count(const uint32_t* __restrict__ idx, int64_t R, int E, int W, int CH,
+                       int32_t* __restrict__ hist, unsigned* status) {
+  extern __shared__ int32_t disp_smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int wg = blockIdx.x * kDispWarps + warp;
+  if (wg >= W) return;
+  int32_t* h = disp_smem + warp * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  const int64_t s0 = (int64_t)wg * CH, s1 = (R < s0 + CH) ? R : s0 + CH;
+  bool bad = false;
+  for (int64_t base = s0; base < s1; base += 32) {
+    const int64_t s = base + lane;
+    const bool act = s < s1;
+    const uint32_t e = act ? idx[s] : 0xFFFFFFFFu;
+    const bool valid = act && e < (uint32_t)E;
+    bad |= act && !valid;
+    const uint32_t key = valid ? e : 0xFFFFFFFFu;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
+    if (valid && lane == __ffs(peers) - 1) h[e] += __popc(peers);
+    __syncwarp();
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(status, kStatusIndex);
+  for (int e = lane; e < E; e += 32) hist[(int64_t)wg * E + e] = h[e];
+}
+
+// One block of kMaxE threads; thread e owns expert e.
+__global__ void __launch_bounds__(kMaxE)
+    moe_dispatch_scan(int32_t* __restrict__ hist, int W, int E, int32_t* __restrict__ offsets) {
+  __shared__ int32_t warp_tot[kMaxE / 32];
+  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+  int32_t run = 0;
+  if (e < E) {
+    int w = 0;
+    for (; w + 4 <= W; w += 4) {  // four independent loads in flight per step
+      const int32_t c0 = hist[(int64_t)(w + 0) * E + e], c1 = hist[(int64_t)(w + 1) * E + e];
+      const int32_t c2 = hist[(int64_t)(w + 2) * E + e], c3 = hist[(int64_t)(w + 3) * E + e];
+      hist[(int64_t)(w + 0) * E + e] = run;
+      hist[(int64_t)(w + 1) * E + e] = run + c0;
+      hist[(int64_t)(w + 2) * E + e] = run + c0 + c1;
+      hist[(int64_t)(w + 3) * E + e] = run + c0 + c1 + c2;
+      run += c0 + c1 + c2 + c3;
+    }
+    for (; w < W; ++w) {
+      const int32_t c = hist[(int64_t)w * E + e];
+      hist[(int64_t)w * E + e] = run;
+      run += c;
+    }
+  }
+  // exclusive scan of the per-expert totals
+  int32_t x = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int32_t t = warp_tot[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xFFFFFFFFu, t, o);
+      if (lane >= o) t += y;
+    }
+    warp_tot[lane] = t;  // inclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int32_t before = (warp > 0 ? warp_tot[warp - 1] : 0) + x - run;
+  if (e < E) offsets[e] = before;
+  if (e == E - 1) offsets[E] = before + run;
+}
+
+__global__ void __launch_bounds__(kDispWarps * 32)
+    moe_dispatch_scatter(const uint32_t* __restrict__ idx, int64_t R, int E, int k, int W, int CH,
+                         const int32_t* __restrict__ hist, const int32_t* __restrict__ offsets,
+                         uint32_t* __restrict__ token_of_row, uint32_t* __restrict__ row_of_slot) {
+  extern __shared__ int32_t disp_smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int wg = blockIdx.x * kDispWarps + warp;
+  if (wg >= W) return;
+  int32_t* run = disp_smem + warp * E;
+  for (int e = lane; e < E; e += 32) run[e] = offsets[e] + hist[(int64_t)wg * E + e];
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  const int64_t s0 = (int64_t)wg * CH, s1 = (R < s0 + CH) ? R : s0 + CH;
+  for (int64_t base = s0; base < s1; base += 32) {
+    const int64_t s = base + lane;
+    const bool act = s < s1;
+    const uint32_t e = act ? idx[s] : 0xFFFFFFFFu;
+    const bool valid = act && e < (uint32_t)E;
+    const uint32_t key = valid ? e : 0xFFFFFFFFu;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, key);
+    if (valid) {
+      const uint32_t row = (uint32_t)(run[e] + __popc(peers & lt));
+      row_of_slot[s] = row;
+      token_of_row[row] = (uint32_t)(s / k);
+    } else if (act) {
+      row_of_slot[s] = kInvalidRow;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) run[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// One block per token (grid-stride): x[t] is read once and written to its k dispatched rows.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS)
+    moe_dispatch_rows(const uint4* __restrict__ x, int64_t T, int64_t vecs_per_row, int k,
+                      const uint32_t* __restrict__ row_of_slot, uint4* __restrict__ x_d) {
+  extern __shared__ uint32_t rows_smem[];
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    for (int j = threadIdx.x; j < k; j += THREADS) rows_smem[j] = row_of_slot[t * k + j];
+    __syncthreads();
+    const uint4* src = x + t * vecs_per_row;
+    for (int64_t c = threadIdx.x; c < vecs_per_row; c += THREADS) {
+      const uint4 v = ld_nc_v4(src + c);
+      for (int j = 0; j < k; ++j) {
+        const uint32_t r = rows_smem[j];
+        if (r != kInvalidRow) st_v4(x_d + (int64_t)r * vecs_per_row + c, v);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+DispatchPlan dispatch_plan(int64_t R) {
+  DispatchPlan p;
+  int64_t W = (R + 255) / 256;
+  if (W > 1024) W = 1024;
+  if (W < 1) W = 1;
+  int64_t CH = (R + W - 1) / W;
+  CH = (CH + 31) / 32 * 32;
+  if (CH < 32) CH = 32;
+  p.CH = (int)CH;
+  p.W = (int)((R + CH - 1) / CH);
+  if (p.W < 1) p.W = 1;
+  return p;
+}
+
+size_t dispatch_scratch_bytes(int64_t R, int E) {
+  return (size_t)dispatch_plan(R).W * (size_t)E * sizeof(int32_t);
+}
+
+cudaError_t launch_dispatch(const void* x, int xdt, int64_t T, int64_t H, const uint32_t* idx,
+                            int E, int k, void* x_d, int32_t* offsets, uint32_t* token_of_row,
+                            uint32_t* row_of_slot, int32_t* hist, unsigned* status,
+                            cudaStream_t s) {
+  const int64_t R = T * k;
+  const DispatchPlan p = dispatch_plan(R);
+  const size_t smem = (size_t)kDispWarps * E * sizeof(int32_t);
+  const unsigned blocks = (unsigned)((p.W + kDispWarps - 1) / kDispWarps);
+  moe_dispatch_count<<<blocks, kDispWarps * 32, smem, s>>>(idx, R, E, p.W, p.CH, hist, status);
+  moe_dispatch_scan<<<1, kMaxE, 0, s>>>(hist, p.W, E, offsets);
+  moe_dispatch_scatter<<<blocks, kDispWarps * 32, smem, s>>>(idx, R, E, k, p.W, p.CH, hist,
+                                                              offsets, token_of_row, row_of_slot);
+  const size_t esz = xdt == MOE_F32 ? 4 : 2;
+  const int64_t vecs = H * (int64_t)esz / 16;
+  int64_t grid = T < 65536 ? T : 65536;
+  moe_dispatch_rows<128><<<(unsigned)grid, 128, (size_t)k * 4, s>>>(
+      (const uint4*)x, T, vecs, k, row_of_slot, (uint4*)x_d);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

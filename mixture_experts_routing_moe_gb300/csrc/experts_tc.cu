@@ -1,0 +1,489 @@
+// bf16 / f16 SwiGLU experts on 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+// SwiGluExperts::forward_dispatched of the ruDNN user guide, §5 "Expertengewichte und Verteilung":
+//   kernel gate/up:  a[r, i] = silu(x_d[r] . gate[e, i]) * (x_d[r] . up[e, i])   (a stored in wdt)
+//   kernel down:     y[r, h] = a[r] . down[e, h]                                   (y stored in wdt)
+// over the ragged row groups offsets[e] .. offsets[e+1]-1 of the dispatched rows.
+//
+// Both kernels are one persistent CTA per SM with three warp roles:
+//   warp 0     TMA producer: per 64-deep K slice loads a 128-row A tile (x_d or a) and a
+//              256-row B tile into a 4-stage shared-memory ring (128-byte swizzle).  For
+//              gate/up the B tile is 128 rows of gate followed by the same 128 rows of up, so
+//              one N = 256 MMA yields both projections of 128 intermediate columns.
+//   warp 1     MMA issuer (one thread): tcgen05.mma kind::f16, M = 128, N = 256, K = 16, FP32
+//              accumulators in TMEM, double-buffered (2 x 256 of the 512 columns) so the epilogue
+//              of one tile overlaps the MMAs of the next.  tcgen05.commit frees ring slots.
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator (each warp reads its 32-lane quarter =
+//              32 tile rows), silu(g) * u (gate/up) or plain cast (down), 16-byte stores, masked
+//              to the expert's rows and to the valid columns.
+// Tiles are (expert, m-tile, n-tile); the list is derived on the device from the offsets.  Within
+// an expert, tiles run in groups of 8 m-tiles, n-tile major, so CTAs working at the same time
+// share weight tiles and activation tiles through L2.
+// Every wait on an mbarrier is bounded (about a second); on expiry the CTA records the timeout in
+// the status word, stops issuing, lets in-flight copies and MMAs land, frees TMEM and exits.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tiles.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, GM = 8;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr long long kWaitLimit = 2000000000LL;  // SM clock cycles
+constexpr int kMaxExperts = 1024;
+constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_BYTES +
+                              256 /*barriers, flags*/ + (kMaxExperts + 4) * sizeof(int);
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of `bar`.  Gives up when another role has given up (abort flag) or
+// after kWaitLimit cycles, in which case it raises the abort flag and the timeout status bit.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_f,
+                                             unsigned* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_f) return false;
+    if (clock64() - t0 > kWaitLimit) {
+      *abort_f = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+// Bounded wait that ignores the abort flag (used only while draining after an abort).
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kWaitLimit) {
+  }
+}
+
+__device__ __forceinline__ void tma_prefetch(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: FP32 accumulator, A and B of the same 16-bit
+// type (bf16 or f16), both K-major, dense; N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(bool bf16, int M, int N) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// Shared-memory matrix descriptor for a K-major tile written by TMA with 128-byte swizzle:
+// rows of 128 bytes, 8-row (1024-byte) core groups strided by SBO = 1024 bytes.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void decode_tile(int t, const int* pref, int E, int NT, int& e, int& m,
+                                            int& n) {
+  e = find_expert(pref, E, t / NT);
+  const int local = t - pref[e] * NT;
+  const int mt = pref[e + 1] - pref[e];
+  const int grp = local / (GM * NT);
+  const int gm = min(GM, mt - grp * GM);
+  const int r = local - grp * GM * NT;
+  n = r / gm;
+  m = grp * GM + r % gm;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if (BF16) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+struct TcParams {
+  const int32_t* offsets;
+  uint8_t* out;       // a [rows, N] (gate/up) or y [rows, N] (down), 16-bit elements
+  unsigned* status;
+  int E;
+  int N;              // valid output columns: I (gate/up) or H (down)
+  int KB;             // 64-deep K slices: ceil(H / 64) or ceil(I / 64)
+  int NT;             // n-tiles per expert: ceil(I / 128) or ceil(H / 256)
+  int b_rows;         // rows of the B tensor per expert: I or H
+};
+
+template <bool GATEUP, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_experts_tc(const __grid_constant__ CUtensorMap mapA,
+                   const __grid_constant__ CUtensorMap mapB0,
+                   const __grid_constant__ CUtensorMap mapB1, const TcParams p) {
+  extern __shared__ uint8_t tc_smem_raw[];
+  const uint32_t raw = smem_u32(tc_smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = tc_smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* pref = reinterpret_cast<int*>(tmem_slot + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_f = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (warp == 2) build_mtile_prefix(p.offsets, p.E, BM, pref, lane);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&mapA);
+    tma_prefetch(&mapB0);
+    if (GATEUP) tma_prefetch(&mapB1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = pref[p.E] * p.NT;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int stage = 0, armed = 0;
+      uint32_t phase = 0;
+      bool stop = false;
+      for (int t = blockIdx.x; t < total && !stop; t += gridDim.x) {
+        int e, m, n;
+        decode_tile(t, pref, p.E, p.NT, e, m, n);
+        const int a_row = __ldg(p.offsets + e) + m * BM;
+        const int b_row = e * p.b_rows + n * (GATEUP ? BN / 2 : BN);
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_f, p.status)) {
+            stop = true;
+            break;
+          }
+          const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+          mbar_expect_tx(full_bar(stage), STAGE_BYTES);
+          tma_load_2d(sa, &mapA, full_bar(stage), kb * BK, a_row);
+          if (GATEUP) {
+            tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, b_row);
+            tma_load_2d(sb + B_BYTES / 2, &mapB1, full_bar(stage), kb * BK, b_row);
+          } else {
+            tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, b_row);
+          }
+          ++armed;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort_f) {  // let the copies still in flight land before the CTA exits
+        for (int i = 0; i < min(armed, STAGES); ++i) {
+          if (stage == 0) {
+            stage = STAGES - 1;
+            phase ^= 1u;
+          } else {
+            --stage;
+          }
+          wait_drain(full_bar(stage), phase);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = make_idesc(BF16, BM, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool stop = false;
+      for (int t = blockIdx.x; t < total && !stop; t += gridDim.x) {
+        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_f, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, abort_f, p.status)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+          const uint64_t da = make_sdesc(sa), db = make_sdesc(sb);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 elements = 32 bytes along K
+            umma_f16(d_tmem, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
+          umma_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (stop) break;
+        umma_commit(tfull_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      umma_commit(drain_bar);  // arrives once every MMA issued above has completed
+      wait_drain(drain_bar, 0);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int e, m, n;
+      decode_tile(t, pref, p.E, p.NT, e, m, n);
+      const bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_f, p.status);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      const int row = __ldg(p.offsets + e) + m * BM + q * 32 + lane;
+      const bool valid = row < __ldg(p.offsets + e + 1);
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      uint8_t* orow = p.out + (size_t)row * p.N * 2;
+      if (GATEUP) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c * 32, g);
+          tmem_ld32(taddr + BN / 2 + c * 32, u);
+          tmem_wait_ld();
+          const int col0 = n * (BN / 2) + c * 32;
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (col0 + v * 8 < p.N) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  float a2[2];
+#pragma unroll
+                  for (int h = 0; h < 2; ++h) {
+                    const float gv = __uint_as_float(g[v * 8 + i * 2 + h]);
+                    const float uv = __uint_as_float(u[v * 8 + i * 2 + h]);
+                    a2[h] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                  }
+                  pk[i] = pack2<BF16>(a2[0], a2[1]);
+                }
+                st_v4(orow + (size_t)(col0 + v * 8) * 2, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+              }
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c * 32, r);
+          tmem_wait_ld();
+          const int col0 = n * BN + c * 32;
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (col0 + v * 8 < p.N) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  pk[i] = pack2<BF16>(__uint_as_float(r[v * 8 + i * 2]),
+                                      __uint_as_float(r[v * 8 + i * 2 + 1]));
+                st_v4(orow + (size_t)(col0 + v * 8) * 2, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+// 2-D K-major map over a [rows, K] 16-bit matrix, box = 64 (K) x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, bool bf16, int64_t K, int64_t rows, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+             const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool GATEUP, bool BF16>
+cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                       const TcParams& p, int64_t rows, int sms, cudaStream_t s) {
+  cudaError_t err = cudaFuncSetAttribute(moe_experts_tc<GATEUP, BF16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const int64_t upper = ((rows + BM - 1) / BM + p.E) * (int64_t)p.NT;  // >= number of tiles
+  const int grid = (int)(upper < sms ? upper : sms);
+  moe_experts_tc<GATEUP, BF16><<<grid, kThreads, kSmemBytes, s>>>(a, b0, b1, p);
+  return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t launch_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, const void* gate,
+                        const void* up, const void* down, int E, int H, int I, void* y, void* a,
+                        unsigned* status, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+
+  CUtensorMap mx, mg, mu, ma, md;
+  if (!make_map(&mx, x_d, BF16, H, rows, BM) || !make_map(&mg, gate, BF16, H, (int64_t)E * I, BN / 2) ||
+      !make_map(&mu, up, BF16, H, (int64_t)E * I, BN / 2) || !make_map(&ma, a, BF16, I, rows, BM) ||
+      !make_map(&md, down, BF16, I, (int64_t)E * H, BN))
+    return cudaErrorInvalidValue;
+
+  TcParams p1{offsets, (uint8_t*)a, status, E, I, (H + BK - 1) / BK, (I + BN / 2 - 1) / (BN / 2), I};
+  err = launch_one<true, BF16>(mx, mg, mu, p1, rows, sms, s);
+  if (err != cudaSuccess) return err;
+  TcParams p2{offsets, (uint8_t*)y, status, E, H, (I + BK - 1) / BK, (H + BN - 1) / BN, H};
+  return launch_one<false, BF16>(ma, md, md, p2, rows, sms, s);
+}
+
+}  // namespace
+
+cudaError_t launch_experts_tc(const void* x_d, const int32_t* offsets, int64_t rows,
+                              const void* gate, const void* up, const void* down, int wdt, int E,
+                              int H, int I, void* y, void* a, unsigned* status, cudaStream_t s) {
+  if (wdt == MOE_BF16)
+    return launch_tc_t<true>(x_d, offsets, rows, gate, up, down, E, H, I, y, a, status, s);
+  if (wdt == MOE_F16)
+    return launch_tc_t<false>(x_d, offsets, rows, gate, up, down, E, H, I, y, a, status, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -1,0 +1,42 @@
+// Internal launchers of libmoe (not part of the C ABI).  Each returns the CUDA error of its
+// launches; arguments are validated by the entry points in api.cu before these run.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// status word bits (device side), reported by moe_device_status()
+constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kStatusIndex = 2u;
+
+cudaError_t launch_route(const void* logits, int ldt, int64_t T, int E, int k, int renorm,
+                         uint32_t* idx, void* w, cudaStream_t s);
+
+// Dispatch splits the R = T*k slots into W contiguous chunks of CH slots, one per warp.
+struct DispatchPlan {
+  int W;   // chunks (warps)
+  int CH;  // slots per chunk, a multiple of 32
+};
+DispatchPlan dispatch_plan(int64_t R);
+size_t dispatch_scratch_bytes(int64_t R, int E);  // per-chunk histograms
+cudaError_t launch_dispatch(const void* x, int xdt, int64_t T, int64_t H, const uint32_t* idx,
+                            int E, int k, void* x_d, int32_t* offsets, uint32_t* token_of_row,
+                            uint32_t* row_of_slot, int32_t* hist, unsigned* status,
+                            cudaStream_t s);
+
+cudaError_t launch_combine(const void* y, int ydt, const uint32_t* row_of_slot, const void* w,
+                           int wdt, int64_t T, int64_t H, int k, void* out, cudaStream_t s);
+
+// f32 experts on CUDA cores; `a` is an [rows, I] f32 scratch buffer.
+cudaError_t launch_experts_simt(const float* x_d, const int32_t* offsets, int64_t rows,
+                                const float* gate, const float* up, const float* down, int E,
+                                int H, int I, float* y, float* a, cudaStream_t s);
+
+// bf16 / f16 experts on tcgen05 tensor cores; `a` is an [rows, I] scratch buffer of dtype wdt.
+cudaError_t launch_experts_tc(const void* x_d, const int32_t* offsets, int64_t rows,
+                              const void* gate, const void* up, const void* down, int wdt, int E,
+                              int H, int I, void* y, void* a, unsigned* status, cudaStream_t s);
+
+}  // namespace moe
