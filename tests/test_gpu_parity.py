@@ -146,9 +146,14 @@ def test_combine_matches_oracle(ydt, wdt, T, k, H):
     rounded = O.round_to_dtype(ref, DT_NAME[ydt])
     if ydt == torch.float32:
         np.testing.assert_allclose(got[fin], ref[fin], rtol=1e-5, atol=1e-5)
-    else:   # FP32 sum then one rounding: within one step of the correctly rounded value
+    else:
+        # FP32 sum then one rounding: within one step of the correctly rounded value, or (where
+        # cancellation leaves a result in f16's subnormal range) within the FP32 accumulation
+        # error bound k * 2^-23 * sum_j |w_j y_j|
         from gpu_helpers import ulp_distance
-        assert ulp_distance(out, rounded)[fin].max() <= 1
+        mag = O.combine(np.abs(O.to_f64(*storage(y))), r_of_s, np.abs(O.to_f64(*storage(w))))
+        ok = (ulp_distance(out, rounded) <= 1) | (np.abs(got - ref) <= k * 2.0 ** -23 * mag)
+        assert ok[fin].all()
 
 
 # ------------------------------------------------------------------------------------ experts
