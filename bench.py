@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Benchmark of the local MoE forward (route -> dispatch -> SwiGLU experts -> combine) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one moe_forward over the workload's whole batch (all four stages), inputs resident in
+HBM.  Prints ONE JSON line on rank 0.  Default workload: the many-expert skewed layer (T=16384,
+H=7168, I=2048, E=256, top_k=8, bf16, Zipf(1.2) expert bias) -- the largest full-layer workload;
+the route-only sweep is not a full forward.  Inputs and weights are larger than L2 (x 235 MB,
+weights 22.5 GB), so no L2 flush is needed between steps.
+
+The path shards only as independent replicas (every token is independent given replicated expert
+weights), so under torchrun each rank runs its own batch: weak scaling, no collective on the data
+path; the timed region is bracketed by barriers and the max over ranks is reported.
+
+--impl reference times the fp64 CPU oracle (the only reference implementation of this method; the
+pages publish no code to install) on rank 0, on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from mixture_experts_routing_moe_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MoE fwd tokens/s; grouped-GEMM TFLOP/s vs bf16 peak; route/combine GB/s vs HBM"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS_PER_FORWARD = 8   # route 1, dispatch 4 (count, scan, scatter, rows), experts 2, combine 1
+STAGES = ["route", "dispatch", "gate_up_gemm", "down_gemm", "combine"]
+# DRAM traffic of one gate/up GEMM launch on the skewed workload, from the ncu capture summarised
+# in profiles/gateup_tc_skewed.md, valid while experts_tc.cu has the recorded hash.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gateup_tc_skewed.md")
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="skewed",
+                    choices=sorted(k for k, v in W.WORKLOADS.items() if v.H > 0))
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------ environment
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            flat = {}
+
+            def walk(o, pre=""):
+                if isinstance(o, dict):
+                    for k, v in o.items():
+                        walk(v, f"{pre}{k}.")
+                elif isinstance(o, (int, float)):
+                    flat[pre[:-1]] = float(o)
+            walk(d)
+
+            def pick(*names):
+                for n in names:
+                    for k, v in flat.items():
+                        if k.split(".")[-1] == n:
+                            return v
+                return None
+            p = {"hbm_gbs": pick("hbm_gbs", "hbm_GBs", "copy_gbs"),
+                 "bf16_tflops": pick("bf16_tflops", "bf16_tflops_burst"),
+                 "bf16_tflops_sustained": pick("bf16_tflops_sustained")}
+            if p["hbm_gbs"] and p["bf16_tflops"]:
+                if not p["bf16_tflops_sustained"]:
+                    p["bf16_tflops_sustained"] = p["bf16_tflops"]
+                return p, "measured"
+        except Exception as e:  # malformed file: fall back, say so
+            log(f"MEASURED_PEAKS.json unreadable ({e}); using fallback peaks")
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device):
+        self.proc = None
+        self.path = None
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            self.uuid = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}",
+               "--format=csv,noheader,nounits", "-lms", "100"]
+        if self.uuid:
+            u = self.uuid if self.uuid.startswith("GPU-") else f"GPU-{self.uuid}"
+            cmd += ["-i", u]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------------------ work accounting
+def stage_work(wl: W.Workload, n_active: int):
+    """Algorithmic bytes / flops of one forward, per stage (the roofline numerators)."""
+    es = 2 if wl.dtype != "f32" else 4
+    T, E, H, I, k = wl.T, wl.E, wl.H, wl.I, wl.top_k
+    R = T * k
+    return {
+        "route": {"bytes": T * E * es + R * (4 + es)},
+        "dispatch": {"bytes": T * H * es + R * H * es + 3 * R * 4},
+        "gate_up_gemm": {"flops": 4 * R * H * I,
+                         "bytes": R * H * es + 2 * n_active * I * H * es + R * I * es},
+        "down_gemm": {"flops": 2 * R * I * H,
+                      "bytes": R * I * es + n_active * H * I * es + R * H * es},
+        "combine": {"bytes": R * H * es + R * (4 + es) + T * H * es},
+    }
+
+
+def recorded_traffic():
+    """(bytes per launch, kernel hash) from the committed ncu summary, or None."""
+    try:
+        txt = open(TRAFFIC_FILE).read()
+    except OSError:
+        return None
+    want = {}
+    for line in txt.splitlines():
+        if line.startswith("traffic_bytes_per_full_launch:"):
+            want["bytes"] = float(line.split(":", 1)[1])
+        if line.startswith("kernel_source_sha256:"):
+            want["sha"] = line.split(":", 1)[1].strip()
+    src = os.path.join(ROOT, "mixture_experts_routing_moe_gb300", "csrc", "experts_tc.cu")
+    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if "bytes" in want and want.get("sha") == cur:
+        return want["bytes"]
+    return None
+
+
+# ------------------------------------------------------------------------------ oracle timing
+def oracle_sample(wl, host, tokens):
+    """Run the fp64 oracle end to end (route + dispatch + experts + combine) on `tokens`."""
+    import oracle as O
+    name = wl.dtype
+    l64 = O.to_f64(host["logits"][tokens], name)
+    idx, w = O.route(l64, wl.top_k, wl.renormalize, name)
+    x64 = O.to_f64(host["x"][tokens], name)
+
+    def weights(e):
+        return tuple(O.to_f64(host[m][e], name) for m in ("gate", "up", "down"))
+    return O.forward_rows(x64, idx, w, weights)
+
+
+def host_storage(inp):
+    return {k: W.to_storage_numpy(v)[0] for k, v in inp.items()}
+
+
+def time_oracle(wl, host, seconds: float, first_token: int = 0):
+    """Oracle throughput on a bounded sample: grow the token sample until ~`seconds` of CPU work."""
+    n, done, elapsed = 1, 0, 0.0
+    t_first = first_token
+    while elapsed < seconds and done < wl.T:
+        n = min(n, wl.T - done)
+        toks = (np.arange(n) + t_first) % wl.T
+        t0 = time.perf_counter()
+        oracle_sample(wl, host, toks)
+        dt = time.perf_counter() - t0
+        elapsed += dt
+        done += n
+        t_first += n
+        if dt < seconds / 8:
+            n *= 2
+    return done, elapsed
+
+
+# ------------------------------------------------------------------------------ arms
+def run_reference(args):
+    rank, world, local = dist_setup()
+    if rank != 0:
+        return
+    wl = W.WORKLOADS[args.workload]
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    inp = W.make_layer_inputs(wl, dev)
+    host = host_storage(inp)
+    del inp
+    # per-step sample sized so the whole --warmup + --steps run stays near 90 s of CPU time
+    t0 = time.perf_counter()
+    oracle_sample(wl, host, np.array([0]))
+    per_token = max(time.perf_counter() - t0, 1e-4)
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    S = int(max(1, min(wl.T, budget // per_token)))
+    tok = 0
+    for _ in range(args.warmup):
+        oracle_sample(wl, host, (np.arange(S) + tok) % wl.T)
+        tok += S
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_sample(wl, host, (np.arange(S) + tok) % wl.T)
+        tok += S
+    el = time.perf_counter() - t0
+    value = S * args.steps / el
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                       "top_k": wl.top_k, "renormalize": wl.renormalize, "storage_dtype": wl.dtype,
+                       "sample_tokens_per_step": S, "parallelism": "rank 0 only"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{S} token(s) per step of the {wl.name} workload, fp64 "
+                                       f"numpy oracle end to end, BLAS on all {cores} host cores"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import mixture_experts_routing_moe_gb300 as moe
+    from mixture_experts_routing_moe_gb300 import build as build_mod
+    build_mod.build()
+    rank, world, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream()
+    inp = W.make_layer_inputs(wl, dev)
+    x, logits, gate, up, down = (inp[k] for k in ("x", "logits", "gate", "up", "down"))
+    out = torch.empty_like(x)
+    wsb = moe.forward_workspace_bytes(wl.T, wl.E, wl.H, wl.I, wl.top_k, logits.dtype, x.dtype)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+    idx, _ = moe.moe_route(logits, wl.top_k, wl.renormalize)
+    counts = torch.bincount(idx.view(torch.int32).flatten().long(), minlength=wl.E)
+    n_active = int((counts > 0).sum())
+    max_load = int(counts.max())
+    del idx
+
+    def step(evs=None):
+        if evs is None:
+            moe.moe_forward(x, logits, gate, up, down, wl.top_k, wl.renormalize, out=out, ws=ws)
+        else:
+            moe.moe_forward_with_events(x, logits, gate, up, down, wl.top_k, wl.renormalize, out,
+                                        ws, evs)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    st = moe.moe_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)   # let the sampler take its first reading
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    el_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+    stage_ms = {s: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in evs]))
+                for j, s in enumerate(STAGES)}
+    st = moe.moe_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
+
+    value = wl.T * args.steps * world / (el_ms / 1e3)
+    pk, pk_src = peaks()
+    work = stage_work(wl, n_active)
+    stages = {}
+    for s in STAGES:
+        d = {"ms": stage_ms[s]}
+        if "flops" in work[s]:
+            d["tflops"] = work[s]["flops"] / (stage_ms[s] / 1e3) / 1e12
+        d["gbs"] = work[s]["bytes"] / (stage_ms[s] / 1e3) / 1e9
+        stages[s] = d
+    dom = "gate_up_gemm"
+    achieved = stages[dom]["tflops"]
+    peak = pk["bf16_tflops_sustained"]
+    traffic = recorded_traffic()
+
+    # end to end through the public API: pinned host inputs in, host output back, every step
+    x_h = x.cpu().pin_memory()
+    l_h = logits.cpu().pin_memory()
+    o_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    x_d, l_d = torch.empty_like(x), torch.empty_like(logits)
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        l_d.copy_(l_h, non_blocking=True)
+        moe.moe_forward(x_d, l_d, gate, up, down, wl.top_k, wl.renormalize, out=out, ws=ws)
+        o_h.copy_(out, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e = {"value": wl.T * args.e2e_steps * world / (e2e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": x.numel() * x.element_size() + logits.numel() * logits.element_size(),
+           "d2h_bytes_per_step": out.numel() * out.element_size()}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        host = host_storage(inp)
+        done, secs = time_oracle(wl, host, args.cpu_seconds)
+        cores = os.cpu_count()
+        cpu = {"value": done / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"first {done} tokens of the {wl.name} workload through the fp64 numpy "
+                         f"oracle end to end ({secs:.1f} s; BLAS threads = all {cores} host cores)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": f"{wl.name}: T={wl.T} H={wl.H} I={wl.I} E={wl.E} "
+                                   f"top_k={wl.top_k} renormalize={wl.renormalize} {wl.dtype}"
+                                   + (f" Zipf({wl.zipf_s}) expert bias" if wl.zipf_s else ""),
+                       "tokens_per_step_per_gpu": wl.T, "active_experts": n_active,
+                       "max_rows_per_expert": max_load,
+                       "l2": "inputs larger than L2 (x %.0f MB, weights %.1f GB); no flush" % (
+                           x.numel() * 2 / 1e6, 3 * gate.numel() * 2 / 1e9),
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"kernel": "moe_experts_tc<gate/up> (tcgen05 grouped GEMM + SwiGLU)",
+                         "bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{pk_src} bf16 sustained",
+                         "traffic": traffic,
+                         "algorithmic_flops_per_launch": work[dom]["flops"],
+                         "algorithmic_bytes_per_launch": work[dom]["bytes"]},
+            "stages": stages,
+            "hbm_peak_gbs": pk["hbm_gbs"],
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": KERNELS_PER_FORWARD * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

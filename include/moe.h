@@ -143,6 +143,18 @@ int moe_forward(const void* x, const void* logits, int ldt, const void* gate, co
                 int renormalize, void* out, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_forward_with_events — moe_forward that also records caller-created CUDA events
+ * (cudaEvent_t, passed as void*) on `stream` at the stage boundaries, for timing:
+ *   events[0] before the route      events[1] after the route     events[2] after dispatch
+ *   events[3] after the gate/up GEMM events[4] after the down GEMM events[5] after the combine
+ * `events` may be NULL (then this is moe_forward).  The launched work is identical.
+ */
+int moe_forward_with_events(const void* x, const void* logits, int ldt, const void* gate,
+                            const void* up, const void* down, int wdt, int64_t T, int64_t E,
+                            int64_t H, int64_t I, int top_k, int renormalize, void* out, void* ws,
+                            size_t ws_bytes, moe_stream_t stream, void* const* events);
+
+/*
  * moe_device_status — synchronises `stream`, then reads and clears the status word at the start
  * of a workspace used by moe_dispatch, moe_experts_forward_dispatched or moe_forward.
  * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_INDEX, or MOE_ERR_CUDA if the read itself failed.

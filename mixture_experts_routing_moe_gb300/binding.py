@@ -38,6 +38,8 @@ _SIGS = {
     "moe_forward_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _int, _int, _int]),
     "moe_forward": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _int, _i64, _i64, _i64, _i64, _int, _int,
                            _vp, _vp, _sz, _vp]),
+    "moe_forward_with_events": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _int, _i64, _i64, _i64,
+                                       _i64, _int, _int, _vp, _vp, _sz, _vp, _vp]),
     "moe_device_status": (_int, [_vp, _sz, _vp]),
 }
 
@@ -194,6 +196,21 @@ def moe_forward(x, logits, gate, up, down, top_k: int, renormalize: bool = True,
     _check(lib().moe_forward(_ptr(x), _ptr(logits), _code(logits), _ptr(gate), _ptr(up),
                              _ptr(down), _code(gate), T, E, H, I, top_k, int(bool(renormalize)),
                              _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "moe_forward")
+    return out
+
+
+def moe_forward_with_events(x, logits, gate, up, down, top_k: int, renormalize: bool, out, ws,
+                            events, stream=None):
+    """moe_forward recording six torch.cuda.Event objects at the stage boundaries
+    (before route / after route / after dispatch / after gate-up / after down / after combine)."""
+    _cuda(x, logits, gate, up, down, out, ws)
+    T, H = x.shape
+    E, I, _ = gate.shape
+    arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
+    _check(lib().moe_forward_with_events(
+        _ptr(x), _ptr(logits), _code(logits), _ptr(gate), _ptr(up), _ptr(down), _code(gate), T, E,
+        H, I, top_k, int(bool(renormalize)), _ptr(out), _ptr(ws), ws.numel(), _stream(stream),
+        arr), "moe_forward_with_events")
     return out
 
 

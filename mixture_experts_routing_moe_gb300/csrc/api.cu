@@ -69,13 +69,18 @@ int check_experts_shape(int64_t rows, int64_t E, int64_t H, int64_t I) {
 
 int run_experts(const void* x_d, const int32_t* offsets, int64_t rows, const void* gate,
                 const void* up, const void* down, int wdt, int64_t E, int64_t H, int64_t I,
-                void* y, void* a, unsigned* status, cudaStream_t s) {
+                void* y, void* a, unsigned* status, cudaStream_t s, cudaEvent_t between = nullptr) {
   if (wdt == MOE_F32)
     return cuda_status(launch_experts_simt((const float*)x_d, offsets, rows, (const float*)gate,
                                            (const float*)up, (const float*)down, (int)E, (int)H,
-                                           (int)I, (float*)y, (float*)a, s));
+                                           (int)I, (float*)y, (float*)a, s, between));
   return cuda_status(launch_experts_tc(x_d, offsets, rows, gate, up, down, wdt, (int)E, (int)H,
-                                       (int)I, y, a, status, s));
+                                       (int)I, y, a, status, s, between));
+}
+
+// Records events[i] on s when an event array is given.
+bool record(void* const* events, int i, cudaStream_t s) {
+  return !events || cudaEventRecord((cudaEvent_t)events[i], s) == cudaSuccess;
 }
 
 }  // namespace
@@ -188,6 +193,14 @@ size_t moe_forward_workspace_bytes(int64_t T, int64_t E, int64_t H, int64_t I, i
 int moe_forward(const void* x, const void* logits, int ldt, const void* gate, const void* up,
                 const void* down, int wdt, int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
                 int renormalize, void* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return moe_forward_with_events(x, logits, ldt, gate, up, down, wdt, T, E, H, I, top_k,
+                                 renormalize, out, ws, ws_bytes, stream, nullptr);
+}
+
+int moe_forward_with_events(const void* x, const void* logits, int ldt, const void* gate,
+                            const void* up, const void* down, int wdt, int64_t T, int64_t E,
+                            int64_t H, int64_t I, int top_k, int renormalize, void* out, void* ws,
+                            size_t ws_bytes, moe_stream_t stream, void* const* events) {
   if (!valid_dtype(ldt) || !valid_dtype(wdt)) return MOE_ERR_DTYPE;
   int st = check_route_shape(T, E, top_k);
   if (st != MOE_OK) return st;
@@ -219,13 +232,17 @@ int moe_forward(const void* x, const void* logits, int ldt, const void* gate, co
   const int64_t R = T * top_k;
 
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!record(events, 0, s)) return MOE_ERR_CUDA;
   cudaError_t err = launch_route(logits, ldt, T, (int)E, top_k, renormalize != 0, idx, w, s);
-  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  if (err != cudaSuccess || !record(events, 1, s)) return MOE_ERR_CUDA;
   err = launch_dispatch(x, wdt, T, H, idx, (int)E, top_k, xd, offsets, tor, ros, hist, status, s);
-  if (err != cudaSuccess) return MOE_ERR_CUDA;
-  st = run_experts(xd, offsets, R, gate, up, down, wdt, E, H, I, /*y=*/xd, a, status, s);
-  if (st != MOE_OK) return st;
-  return cuda_status(launch_combine(xd, wdt, ros, w, ldt, T, H, top_k, out, s));
+  if (err != cudaSuccess || !record(events, 2, s)) return MOE_ERR_CUDA;
+  st = run_experts(xd, offsets, R, gate, up, down, wdt, E, H, I, /*y=*/xd, a, status, s,
+                   events ? (cudaEvent_t)events[3] : nullptr);
+  if (st != MOE_OK || !record(events, 4, s)) return st != MOE_OK ? st : MOE_ERR_CUDA;
+  err = launch_combine(xd, wdt, ros, w, ldt, T, H, top_k, out, s);
+  if (err != cudaSuccess || !record(events, 5, s)) return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 int moe_device_status(void* ws, size_t ws_bytes, moe_stream_t stream) {

@@ -91,10 +91,15 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_experts_simt(const float* x_d, const int32_t* offsets, int64_t rows,
                                 const float* gate, const float* up, const float* down, int E,
-                                int H, int I, float* y, float* a, cudaStream_t s) {
+                                int H, int I, float* y, float* a, cudaStream_t s,
+                                cudaEvent_t between) {
   const int64_t mtiles = (rows + SB - 1) / SB + E;  // upper bound of sum_e ceil(n_e / 64)
   dim3 g1((unsigned)mtiles, (unsigned)((I + SB - 1) / SB));
   moe_experts_simt<true><<<g1, 256, 0, s>>>(x_d, offsets, E, H, I, gate, up, a);
+  if (between) {
+    const cudaError_t err = cudaEventRecord(between, s);
+    if (err != cudaSuccess) return err;
+  }
   dim3 g2((unsigned)mtiles, (unsigned)((H + SB - 1) / SB));
   moe_experts_simt<false><<<g2, 256, 0, s>>>(a, offsets, E, I, H, down, nullptr, y);
   return cudaGetLastError();

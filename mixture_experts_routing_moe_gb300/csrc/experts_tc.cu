@@ -454,7 +454,7 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
 template <bool BF16>
 cudaError_t launch_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, const void* gate,
                         const void* up, const void* down, int E, int H, int I, void* y, void* a,
-                        unsigned* status, cudaStream_t s) {
+                        unsigned* status, cudaStream_t s, cudaEvent_t between) {
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
@@ -470,6 +470,7 @@ cudaError_t launch_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, c
   TcParams p1{offsets, (uint8_t*)a, status, E, I, (H + BK - 1) / BK, (I + BN / 2 - 1) / (BN / 2), I};
   err = launch_one<true, BF16>(mx, mg, mu, p1, rows, sms, s);
   if (err != cudaSuccess) return err;
+  if (between && (err = cudaEventRecord(between, s)) != cudaSuccess) return err;
   TcParams p2{offsets, (uint8_t*)y, status, E, H, (I + BK - 1) / BK, (H + BN - 1) / BN, H};
   return launch_one<false, BF16>(ma, md, md, p2, rows, sms, s);
 }
@@ -478,11 +479,14 @@ cudaError_t launch_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, c
 
 cudaError_t launch_experts_tc(const void* x_d, const int32_t* offsets, int64_t rows,
                               const void* gate, const void* up, const void* down, int wdt, int E,
-                              int H, int I, void* y, void* a, unsigned* status, cudaStream_t s) {
+                              int H, int I, void* y, void* a, unsigned* status, cudaStream_t s,
+                              cudaEvent_t between) {
   if (wdt == MOE_BF16)
-    return launch_tc_t<true>(x_d, offsets, rows, gate, up, down, E, H, I, y, a, status, s);
+    return launch_tc_t<true>(x_d, offsets, rows, gate, up, down, E, H, I, y, a, status, s,
+                             between);
   if (wdt == MOE_F16)
-    return launch_tc_t<false>(x_d, offsets, rows, gate, up, down, E, H, I, y, a, status, s);
+    return launch_tc_t<false>(x_d, offsets, rows, gate, up, down, E, H, I, y, a, status, s,
+                              between);
   return cudaErrorInvalidValue;
 }
 

@@ -32,11 +32,13 @@ cudaError_t launch_combine(const void* y, int ydt, const uint32_t* row_of_slot, 
 // f32 experts on CUDA cores; `a` is an [rows, I] f32 scratch buffer.
 cudaError_t launch_experts_simt(const float* x_d, const int32_t* offsets, int64_t rows,
                                 const float* gate, const float* up, const float* down, int E,
-                                int H, int I, float* y, float* a, cudaStream_t s);
+                                int H, int I, float* y, float* a, cudaStream_t s,
+                                cudaEvent_t between = nullptr);
 
 // bf16 / f16 experts on tcgen05 tensor cores; `a` is an [rows, I] scratch buffer of dtype wdt.
 cudaError_t launch_experts_tc(const void* x_d, const int32_t* offsets, int64_t rows,
                               const void* gate, const void* up, const void* down, int wdt, int E,
-                              int H, int I, void* y, void* a, unsigned* status, cudaStream_t s);
+                              int H, int I, void* y, void* a, unsigned* status, cudaStream_t s,
+                              cudaEvent_t between = nullptr);
 
 }  // namespace moe
