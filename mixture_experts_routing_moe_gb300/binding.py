@@ -206,6 +206,11 @@ def moe_forward_with_events(x, logits, gate, up, down, top_k: int, renormalize: 
     _cuda(x, logits, gate, up, down, out, ws)
     T, H = x.shape
     E, I, _ = gate.shape
+    if len(events) != 6:
+        raise ValueError("moe_forward_with_events needs six events")
+    for ev in events:
+        if ev.cuda_event == 0:      # torch creates the CUDA event on its first record
+            ev.record(torch.cuda.current_stream() if stream is None else stream)
     arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
     _check(lib().moe_forward_with_events(
         _ptr(x), _ptr(logits), _code(logits), _ptr(gate), _ptr(up), _ptr(down), _code(gate), T, E,

@@ -61,6 +61,10 @@ WORKLOADS = {
                         dtype="bf16", seed=4),
     "skewed": Workload("skewed", T=16384, H=7168, I=2048, E=256, top_k=8, renormalize=True,
                        dtype="bf16", seed=5, zipf_s=1.2),
+    # profiling case: the skewed layer's expert shape with 32 experts and 2048 tokens, small
+    # enough (2.8 GB of weights) for multi-pass counter captures
+    "skewed_e32": Workload("skewed_e32", T=2048, H=7168, I=2048, E=32, top_k=8,
+                           renormalize=True, dtype="bf16", seed=6, zipf_s=1.2),
 }
 
 
