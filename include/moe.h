@@ -97,6 +97,29 @@ int moe_dispatch(const void* x, int xdt, int64_t T, int64_t H, const uint32_t* i
                  uint32_t* row_of_slot, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_dispatch_static — moe_dispatch without a workspace argument.  The ruDNN pages have no
+ * counterpart: this entry point exists for callers that cannot provide device scratch memory,
+ * such as a plugin whose interface hands over only inputs and outputs, or a runtime whose memory
+ * plan fixes every device allocation at start-up and offers none per call.
+ *
+ * Same arguments, results and alignment rules as moe_dispatch, minus (ws, ws_bytes).  Its scratch
+ * (a status word and the per-chunk histograms) lives in a file-scope device array of
+ * MOE_STATIC_DISPATCH_SCRATCH_BYTES = 256 + 1 MiB that every GPU loading the library holds until
+ * the process exits; it allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ * Sizes needing more than that (moe_dispatch_workspace_bytes(T, E, top_k) > the capacity, e.g.
+ * T * top_k = 131072 with E > 512) are rejected with MOE_ERR_SHAPE before anything is enqueued.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress, once per
+ * device, with that device current); make that first call before any stream capture.
+ * All calls share the one array: calls whose work overlaps on the GPU (different streams, or
+ * several host threads) race on it and must be serialised by the caller.  Ids >= E are handled
+ * as in moe_dispatch (row_of_slot 0xFFFFFFFF); the device status word is not exposed.
+ */
+#define MOE_STATIC_DISPATCH_SCRATCH_BYTES (256u + (1u << 20))
+int moe_dispatch_static(const void* x, int xdt, int64_t T, int64_t H, const uint32_t* idx,
+                        int64_t E, int top_k, void* x_d, int32_t* offsets, uint32_t* token_of_row,
+                        uint32_t* row_of_slot, moe_stream_t stream);
+
+/*
  * moe_experts_forward_dispatched — SwiGluExperts::forward_dispatched of §3/§5/§6.
  *
  * For every expert e and every row r in offsets[e] .. offsets[e+1]-1:

@@ -31,6 +31,8 @@ _SIGS = {
     "moe_dispatch_workspace_bytes": (_sz, [_i64, _i64, _int]),
     "moe_dispatch": (_int, [_vp, _int, _i64, _i64, _vp, _i64, _int, _vp, _vp, _vp, _vp, _vp, _sz,
                             _vp]),
+    "moe_dispatch_static": (_int, [_vp, _int, _i64, _i64, _vp, _i64, _int, _vp, _vp, _vp, _vp,
+                                   _vp]),
     "moe_experts_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _int]),
     "moe_experts_forward_dispatched": (_int, [_vp, _vp, _i64, _vp, _vp, _vp, _int, _i64, _i64,
                                               _i64, _vp, _vp, _sz, _vp]),

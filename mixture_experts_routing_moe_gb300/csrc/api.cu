@@ -142,6 +142,28 @@ int moe_dispatch(const void* x, int xdt, int64_t T, int64_t H, const uint32_t* i
                                      token_of_row, row_of_slot, hist, status, s));
 }
 
+int moe_dispatch_static(const void* x, int xdt, int64_t T, int64_t H, const uint32_t* idx,
+                        int64_t E, int top_k, void* x_d, int32_t* offsets, uint32_t* token_of_row,
+                        uint32_t* row_of_slot, moe_stream_t stream) {
+  if (!valid_dtype(xdt)) return MOE_ERR_DTYPE;
+  int st = check_route_shape(T, E, top_k);
+  if (st != MOE_OK) return st;
+  if (H < 1) return MOE_ERR_SHAPE;
+  if (moe_dispatch_workspace_bytes(T, E, top_k) > kStaticDispatchScratchBytes) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!x || !idx || !x_d || !offsets || !token_of_row || !row_of_slot) return MOE_ERR_NULL;
+  if (!aligned16(x) || !aligned16(x_d) || (H * (int64_t)dtype_size(xdt)) % 16 != 0)
+    return MOE_ERR_ALIGN;
+  void* scratch = nullptr;
+  if (static_dispatch_scratch(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned* status = (unsigned*)scratch;  // the count kernel ORs into it: clear it first
+  if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t* hist = (int32_t*)((uint8_t*)scratch + align_up(kWsHeader, 256));
+  return cuda_status(launch_dispatch(x, xdt, T, H, idx, (int)E, top_k, x_d, offsets,
+                                     token_of_row, row_of_slot, hist, status, s));
+}
+
 size_t moe_experts_workspace_bytes(int64_t rows, int64_t E, int64_t H, int64_t I, int wdt) {
   if (!valid_dtype(wdt) || check_experts_shape(rows, E, H, I) != MOE_OK) return 0;
   return align_up(kWsHeader, 256) + align_up((size_t)rows * I * dtype_size(wdt), 256);

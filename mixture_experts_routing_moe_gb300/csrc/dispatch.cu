@@ -15,8 +15,15 @@
 //                row_of_slot[t*k + 0..k-1] of x_d.
 // Expert ids >= E are not dispatched: their row_of_slot is 0xFFFFFFFF and the status word gets
 // the index bit.  No access goes out of bounds for any id value.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
+
+// Scratch of moe_dispatch_static(): a status word (in the first 256 bytes) followed by the
+// per-chunk histograms, in a file-scope device array instead of caller-provided memory.  Every
+// GPU that loads this library holds it until the process exits.
+static __device__ __align__(256) unsigned char g_static_dispatch_scratch[kStaticDispatchScratchBytes];
 
 namespace moe {
 namespace {
@@ -166,6 +173,27 @@ DispatchPlan dispatch_plan(int64_t R) {
   p.W = (int)((R + CH - 1) / CH);
   if (p.W < 1) p.W = 1;
   return p;
+}
+
+cudaError_t static_dispatch_scratch(void** ptr) {
+  // Host code must not use g_static_dispatch_scratch as an address: that name is a host-side
+  // stand-in.  The device address is looked up once per device, with that device current.
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_static_dispatch_scratch);
+    if (err != cudaSuccess) return err;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
 }
 
 size_t dispatch_scratch_bytes(int64_t R, int E) {

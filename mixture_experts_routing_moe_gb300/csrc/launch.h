@@ -5,6 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+// Capacity of moe_dispatch_static()'s file-scope scratch: 256-byte status header + histograms.
+constexpr size_t kStaticDispatchScratchBytes = 256 + (1u << 20);
+
 namespace moe {
 
 // status word bits (device side), reported by moe_device_status()
@@ -25,6 +28,9 @@ cudaError_t launch_dispatch(const void* x, int xdt, int64_t T, int64_t H, const 
                             int E, int k, void* x_d, int32_t* offsets, uint32_t* token_of_row,
                             uint32_t* row_of_slot, int32_t* hist, unsigned* status,
                             cudaStream_t s);
+
+// Device address of that scratch on the current device (looked up on first use per device).
+cudaError_t static_dispatch_scratch(void** ptr);
 
 cudaError_t launch_combine(const void* y, int ydt, const uint32_t* row_of_slot, const void* w,
                            int wdt, int64_t T, int64_t H, int k, void* out, cudaStream_t s);
