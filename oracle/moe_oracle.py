@@ -33,6 +33,17 @@ Readings taken where the page is silent (each is repeated at the function that a
   R7 routing weights are applied in the combine, after the down projection, summed over the
      slots j = 0..k-1 of a token in slot order; the output takes the input dtype.
 
+Group-limited sigmoid routing follows §10 "Gruppenbeschränktes Sigmoid-MoE-Routing" of the same
+page: sigmoid scores, an optional FP32 correction bias that affects the selection only, groups
+scored by their maximum or the sum of their two largest corrected scores, the best
+`selected_groups` groups, then the top_k experts inside them; weights are the uncorrected sigmoid
+values, optionally renormalised, times `scale`; ties prefer smaller ids.  Readings:
+  S1 the selection (sigmoid, correction, group scores, ranking) is decided in float64 on both
+     sides of the comparison, so CPU and GPU take the same decision;
+  S2 slots are ordered by descending corrected score, equal scores lower id first;
+  S3 rows whose corrected scores hold a NaN keep NaN weights and select ids 0..k-1;
+  S4 weights are rounded once to the logits dtype after renormalisation and scaling.
+
 Pins (tests/test_oracle_pins.py) tie each function to something other than itself: closed forms,
 library routines (torch float64 softmax and silu, numpy's float32 cast), brute force on tiny
 inputs, and invariants.  Parity unpinned: R1 for two *different* logits whose FP32 softmax values
@@ -45,7 +56,7 @@ import numpy as np
 __all__ = [
     "DTYPES", "to_f64", "round_to_dtype", "encode", "poisoned_rows", "softmax", "select_topk",
     "route", "dispatch", "gather", "silu", "swiglu", "experts", "combine", "forward",
-    "forward_rows",
+    "forward_rows", "sigmoid", "route_sigmoid_grouped", "forward_sigmoid_grouped",
 ]
 
 DTYPES = ("f32", "f16", "bf16")
@@ -274,3 +285,66 @@ def forward_rows(x_rows: np.ndarray, idx_rows: np.ndarray, w_rows: np.ndarray, e
         if hi > lo:
             y[lo:hi] = swiglu(x_d[lo:hi], *expert_weights(e))
     return combine(y, row_of_slot, w_rows)
+
+
+# --------------------------------------------------------------------------------------------
+# group-limited sigmoid routing (§10 "Gruppenbeschränktes Sigmoid-MoE-Routing")
+# --------------------------------------------------------------------------------------------
+def sigmoid(z: np.ndarray) -> np.ndarray:
+    """sigmoid(z) = 1 / (1 + exp(-z)); exact limits 0 and 1 at -inf and +inf."""
+    with np.errstate(over="ignore"):
+        return 1.0 / (1.0 + np.exp(-z))
+
+
+def route_sigmoid_grouped(logits: np.ndarray, bias, top_k: int, groups: int, selected_groups: int,
+                          group_top_two: bool, renormalize: bool, scale: float, out_dtype: str):
+    """route_sigmoid_grouped(logits, bias, GroupRoutingOptions) -> (indices u32 [T,k], weights).
+
+    s = sigmoid(l); c = s + bias (bias: FP32 [E] or None, selection only).  Experts form `groups`
+    contiguous groups of E / groups; a group scores max(c) over its experts, or the sum of its two
+    largest c with group_top_two.  The `selected_groups` best groups are kept (ties: lower group
+    id), then the top_k experts inside them by c (ties: lower id).  Weights are s of the chosen
+    experts, divided by their sum when renormalising, times scale, rounded to `out_dtype`.
+    """
+    T, E = logits.shape
+    gs = E // groups
+    assert gs * groups == E and 1 <= selected_groups <= groups
+    assert 1 <= top_k <= selected_groups * gs and (gs >= 2 or not group_top_two)
+    s = sigmoid(logits)
+    c = s + (0.0 if bias is None else np.asarray(bias, dtype=np.float64)[None, :])
+    bad = np.isnan(c).any(axis=1)
+    c = np.where(bad[:, None], 0.0, c)
+    srt = -np.sort(-c.reshape(T, groups, gs), axis=2)
+    gscore = srt[:, :, 0] + srt[:, :, 1] if group_top_two else srt[:, :, 0]
+    gsel = np.argsort(-gscore, axis=1, kind="stable")[:, :selected_groups]
+    allowed = np.zeros((T, groups), dtype=bool)
+    np.put_along_axis(allowed, gsel, True, axis=1)
+    allowed = np.repeat(allowed, gs, axis=1)
+    # rank: allowed experts first, then by corrected score descending, then by id ascending
+    ids = np.broadcast_to(np.arange(E), (T, E))
+    order = np.lexsort((ids, -c, ~allowed), axis=1)
+    idx = order[:, :top_k].copy()
+    idx[bad] = np.arange(top_k)
+    w = np.take_along_axis(s, idx, axis=1)
+    if renormalize:
+        with np.errstate(invalid="ignore", divide="ignore"):
+            w = w / w.sum(axis=1, keepdims=True)
+    w = w * scale
+    w[bad] = np.nan
+    return idx.astype(np.uint32), round_to_dtype(w, out_dtype)
+
+
+def forward_sigmoid_grouped(x, x_dtype, logits, logits_dtype, bias, gate, up, down, w_dtype,
+                            top_k, groups, selected_groups, group_top_two, renormalize, scale):
+    """SwiGluExperts::forward_sigmoid_grouped: sigmoid routing, then dispatch, experts, combine."""
+    l64 = to_f64(logits, logits_dtype)
+    x64 = to_f64(x, x_dtype)
+    E = l64.shape[1]
+    b64 = None if bias is None else to_f64(bias, "f32")
+    idx, w = route_sigmoid_grouped(l64, b64, top_k, groups, selected_groups, group_top_two,
+                                   renormalize, scale, logits_dtype)
+    counts, offsets, token_of_row, row_of_slot = dispatch(idx, E)
+    y = experts(gather(x64, token_of_row), offsets, gate, up, down, w_dtype)
+    out = combine(y, row_of_slot, w)
+    return {"idx": idx, "w": w, "counts": counts, "offsets": offsets,
+            "out_unrounded": out, "out": round_to_dtype(out, x_dtype)}
