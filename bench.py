@@ -55,8 +55,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="skewed",
-                    choices=sorted(k for k, v in W.WORKLOADS.items() if v.H > 0))
+    ap.add_argument("--workload", default="skewed", choices=sorted(W.WORKLOADS),
+                    help="a full-layer workload, or route_sweep to time the route stage alone")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
@@ -294,6 +294,51 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_route_only(args):
+    """The route-only workload: moe_route alone, renormalise on and off, against HBM."""
+    import mixture_experts_routing_moe_gb300 as moe
+    from mixture_experts_routing_moe_gb300 import build as build_mod
+    build_mod.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]
+    logits = W.make_logits(wl, dev)
+    idx = torch.empty(wl.T, wl.top_k, dtype=torch.uint32, device=dev)
+    w = torch.empty(wl.T, wl.top_k, dtype=logits.dtype, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # larger than L2
+    es = logits.element_size()
+    nbytes = wl.T * wl.E * es + wl.T * wl.top_k * (4 + es)
+    pk, pk_src = peaks()
+    res = {}
+    for renorm in (True, False):
+        for _ in range(max(3, args.warmup)):
+            moe.moe_route(logits, wl.top_k, renorm, idx=idx, w=w)
+        times = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            moe.moe_route(logits, wl.top_k, renorm, idx=idx, w=w)
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = float(np.mean(times))
+        res["renormalize" if renorm else "plain"] = {"ms": ms, "gbs": nbytes / (ms / 1e3) / 1e9}
+    best = min(res.values(), key=lambda d: d["ms"])
+    line = {"metric": "route GB/s vs HBM (route-only workload)", "value": wl.T / (best["ms"] / 1e3),
+            "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": best["ms"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": f"{wl.name}: logits [{wl.T}, {wl.E}] {wl.dtype}, top_k={wl.top_k}",
+                       "l2": "L2 flushed (256 MB write) before every launch"},
+            "roofline": {"kernel": "moe_route_kernel", "bound": "hbm",
+                         "achieved": best["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": best["gbs"] / pk["hbm_gbs"], "peak_source": pk_src,
+                         "traffic": None, "algorithmic_bytes_per_launch": nbytes},
+            "variants": res, "gpu_launches": 2 * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args):
     import mixture_experts_routing_moe_gb300 as moe
     from mixture_experts_routing_moe_gb300 import build as build_mod
@@ -435,6 +480,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif W.WORKLOADS[args.workload].H == 0:
+        run_route_only(args)
     else:
         run_ours(args)
 

@@ -107,7 +107,7 @@ int moe_dispatch(const void* x, int xdt, int64_t T, int64_t H, const uint32_t* i
  * MOE_STATIC_DISPATCH_SCRATCH_BYTES = 256 + 1 MiB that every GPU loading the library holds until
  * the process exits; it allocates nothing (no cudaMalloc, cudaFree or allocating library call).
  * Sizes needing more than that (moe_dispatch_workspace_bytes(T, E, top_k) > the capacity, e.g.
- * T * top_k = 131072 with E > 512) are rejected with MOE_ERR_SHAPE before anything is enqueued.
+ * T * top_k = 131072 with E = 1024) are rejected with MOE_ERR_SHAPE before anything is enqueued.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress, once per
  * device, with that device current); make that first call before any stream capture.
  * All calls share the one array: calls whose work overlaps on the GPU (different streams, or

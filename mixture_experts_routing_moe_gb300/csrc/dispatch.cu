@@ -6,9 +6,10 @@
 //   1. count   — warp w owns slots [w*CH, w*CH + CH); it histograms its chunk in a warp-private
 //                shared-memory array (lanes with the same expert are merged with match.any) and
 //                writes hist[w][e].
-//   2. scan    — one block: hist[w][e] becomes the exclusive prefix over w (per expert), and
-//                offsets = exclusive prefix over e of the per-expert totals.
-//   3. scatter — warp w walks its chunk again in slot order; a slot's row is
+//   2. scan    — one block per expert: hist[w][e] becomes the exclusive prefix over w, and
+//                totals[e] the expert's row count.
+//   3. scatter — every warp derives offsets = exclusive prefix over e of totals (warp 0 also
+//                writes them out), then walks its chunk again in slot order; a slot's row is
 //                offsets[e] + hist[w][e] + (earlier slots of the chunk with the same expert), the
 //                last term from match.any ranks.  Writes row_of_slot and token_of_row.
 //   4. rows    — one block per token reads x[t] once (16-byte loads) and writes it to the k rows
@@ -58,31 +59,23 @@ __global__ void __launch_bounds__(kDispWarps * 32)
   for (int e = lane; e < E; e += 32) hist[(int64_t)wg * E + e] = h[e];
 }
 
-// One block of kMaxE threads; thread e owns expert e.
-__global__ void __launch_bounds__(kMaxE)
-    moe_dispatch_scan(int32_t* __restrict__ hist, int W, int E, int32_t* __restrict__ offsets) {
-  __shared__ int32_t warp_tot[kMaxE / 32];
-  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-  int32_t run = 0;
-  if (e < E) {
-    int w = 0;
-    for (; w + 4 <= W; w += 4) {  // four independent loads in flight per step
-      const int32_t c0 = hist[(int64_t)(w + 0) * E + e], c1 = hist[(int64_t)(w + 1) * E + e];
-      const int32_t c2 = hist[(int64_t)(w + 2) * E + e], c3 = hist[(int64_t)(w + 3) * E + e];
-      hist[(int64_t)(w + 0) * E + e] = run;
-      hist[(int64_t)(w + 1) * E + e] = run + c0;
-      hist[(int64_t)(w + 2) * E + e] = run + c0 + c1;
-      hist[(int64_t)(w + 3) * E + e] = run + c0 + c1 + c2;
-      run += c0 + c1 + c2 + c3;
-    }
-    for (; w < W; ++w) {
-      const int32_t c = hist[(int64_t)w * E + e];
-      hist[(int64_t)w * E + e] = run;
-      run += c;
-    }
+// One block per expert e: the column hist[0..W-1][e] becomes its exclusive prefix over the
+// chunks (a block-wide scan), and totals[e] receives the column sum.
+constexpr int kScanThreads = 256;
+__global__ void __launch_bounds__(kScanThreads)
+    moe_dispatch_scan(int32_t* __restrict__ hist, int W, int E, int32_t* __restrict__ totals) {
+  __shared__ int32_t warp_tot[kScanThreads / 32];
+  const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int PER = kMaxE / kScanThreads;  // W <= 1024 chunks: up to 4 per thread
+  int32_t v[PER];
+  int32_t local = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int w = tid * PER + i;
+    v[i] = w < W ? hist[(int64_t)w * E + e] : 0;
+    local += v[i];
   }
-  // exclusive scan of the per-expert totals
-  int32_t x = run;
+  int32_t x = local;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
@@ -91,30 +84,54 @@ __global__ void __launch_bounds__(kMaxE)
   if (lane == 31) warp_tot[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int32_t t = warp_tot[lane];
+    int32_t t = lane < kScanThreads / 32 ? warp_tot[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int32_t y = __shfl_up_sync(0xFFFFFFFFu, t, o);
       if (lane >= o) t += y;
     }
-    warp_tot[lane] = t;  // inclusive prefix of warp totals
+    if (lane < kScanThreads / 32) warp_tot[lane] = t;
   }
   __syncthreads();
-  const int32_t before = (warp > 0 ? warp_tot[warp - 1] : 0) + x - run;
-  if (e < E) offsets[e] = before;
-  if (e == E - 1) offsets[E] = before + run;
+  int32_t run = (warp > 0 ? warp_tot[warp - 1] : 0) + x - local;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int w = tid * PER + i;
+    if (w < W) hist[(int64_t)w * E + e] = run;
+    run += v[i];
+  }
+  if (tid == kScanThreads - 1) totals[e] = run;
 }
 
 __global__ void __launch_bounds__(kDispWarps * 32)
     moe_dispatch_scatter(const uint32_t* __restrict__ idx, int64_t R, int E, int k, int W, int CH,
-                         const int32_t* __restrict__ hist, const int32_t* __restrict__ offsets,
-                         uint32_t* __restrict__ token_of_row, uint32_t* __restrict__ row_of_slot) {
+                         const int32_t* __restrict__ hist, const int32_t* __restrict__ totals,
+                         int32_t* __restrict__ offsets, uint32_t* __restrict__ token_of_row,
+                         uint32_t* __restrict__ row_of_slot) {
   extern __shared__ int32_t disp_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int wg = blockIdx.x * kDispWarps + warp;
   if (wg >= W) return;
   int32_t* run = disp_smem + warp * E;
-  for (int e = lane; e < E; e += 32) run[e] = offsets[e] + hist[(int64_t)wg * E + e];
+  // offsets = exclusive prefix of the per-expert totals, recomputed by every warp (E <= 1024)
+  int32_t carry = 0;
+  for (int base = 0; base < E; base += 32) {
+    const int e = base + lane;
+    const int32_t c = e < E ? totals[e] : 0;
+    int32_t x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (e < E) {
+      const int32_t off = carry + x - c;
+      run[e] = off + hist[(int64_t)wg * E + e];
+      if (wg == 0) offsets[e] = off;
+    }
+    carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+  }
+  if (wg == 0 && lane == 0) offsets[E] = carry;
   __syncwarp();
   const unsigned lt = (1u << lane) - 1u;
   const int64_t s0 = (int64_t)wg * CH, s1 = (R < s0 + CH) ? R : s0 + CH;
@@ -196,8 +213,8 @@ cudaError_t static_dispatch_scratch(void** ptr) {
   return cudaSuccess;
 }
 
-size_t dispatch_scratch_bytes(int64_t R, int E) {
-  return (size_t)dispatch_plan(R).W * (size_t)E * sizeof(int32_t);
+size_t dispatch_scratch_bytes(int64_t R, int E) {  // per-chunk histograms + per-expert totals
+  return ((size_t)dispatch_plan(R).W + 1) * (size_t)E * sizeof(int32_t);
 }
 
 cudaError_t launch_dispatch(const void* x, int xdt, int64_t T, int64_t H, const uint32_t* idx,
@@ -209,9 +226,10 @@ cudaError_t launch_dispatch(const void* x, int xdt, int64_t T, int64_t H, const 
   const size_t smem = (size_t)kDispWarps * E * sizeof(int32_t);
   const unsigned blocks = (unsigned)((p.W + kDispWarps - 1) / kDispWarps);
   moe_dispatch_count<<<blocks, kDispWarps * 32, smem, s>>>(idx, R, E, p.W, p.CH, hist, status);
-  moe_dispatch_scan<<<1, kMaxE, 0, s>>>(hist, p.W, E, offsets);
-  moe_dispatch_scatter<<<blocks, kDispWarps * 32, smem, s>>>(idx, R, E, k, p.W, p.CH, hist,
-                                                              offsets, token_of_row, row_of_slot);
+  int32_t* totals = hist + (size_t)p.W * E;
+  moe_dispatch_scan<<<E, kScanThreads, 0, s>>>(hist, p.W, E, totals);
+  moe_dispatch_scatter<<<blocks, kDispWarps * 32, smem, s>>>(
+      idx, R, E, k, p.W, p.CH, hist, totals, offsets, token_of_row, row_of_slot);
   const size_t esz = xdt == MOE_F32 ? 4 : 2;
   const int64_t vecs = H * (int64_t)esz / 16;
   int64_t grid = T < 65536 ? T : 65536;

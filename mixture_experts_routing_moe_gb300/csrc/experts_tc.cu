@@ -4,7 +4,10 @@
 //   kernel down:     y[r, h] = a[r] . down[e, h]                                   (y stored in wdt)
 // over the ragged row groups offsets[e] .. offsets[e+1]-1 of the dispatched rows.
 //
-// Both kernels are one persistent CTA per SM with three warp roles:
+// Two variants share the structure below: a CTA kernel (one 128 x 256 tile per CTA) and a
+// CTA-pair kernel (one 256 x 256 tile per cluster of two CTAs, cta_group::2, see further down);
+// the launcher takes the pair when experts average at least 128 rows.
+// Both kernels are persistent (one CTA per SM) with three warp roles:
 //   warp 0     TMA producer: per 64-deep K slice loads a 128-row A tile (x_d or a) and a
 //              256-row B tile into a 4-stage shared-memory ring (128-byte swizzle).  For
 //              gate/up the B tile is 128 rows of gate followed by the same 128 rows of up, so
@@ -16,8 +19,8 @@
 //              32 tile rows), silu(g) * u (gate/up) or plain cast (down), 16-byte stores, masked
 //              to the expert's rows and to the valid columns.
 // Tiles are (expert, m-tile, n-tile); the list is derived on the device from the offsets.  Within
-// an expert, tiles run in groups of 8 m-tiles, n-tile major, so CTAs working at the same time
-// share weight tiles and activation tiles through L2.
+// an expert the smaller operand (the expert's rows of x_d / a, or its weights) stays resident in
+// L2 (evict_last) while the larger one streams through once (evict_first).
 // Every wait on an mbarrier is bounded (about a second); on expiry the CTA records the timeout in
 // the status word, stops issuing, lets in-flight copies and MMAs land, frees TMEM and exits.
 #include <cuda.h>
@@ -29,7 +32,7 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, GM = 8;
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -95,12 +98,28 @@ __device__ __forceinline__ void tma_prefetch(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                            int x, int y) {
+                                            int x, int y, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
+}
+// L2 eviction policies: the resident operand is kept (evict_last), the streamed one is not.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -162,16 +181,35 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr) {
          ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-__device__ __forceinline__ void decode_tile(int t, const int* pref, int E, int NT, int& e, int& m,
-                                            int& n) {
+// Tile t -> (expert e, m-tile m, n-tile n).  Inside an expert, the operand with fewer bytes
+// (A: mt * 128 rows, B: NT * 256 rows, both K deep) is the one kept resident in L2 while the
+// other streams through once: A resident -> n outer, m inner; B resident -> m outer, n inner.
+// When the resident operand exceeds kResidentBytes it is cut into groups that do fit.
+// Returns true when A is the resident operand.
+constexpr long long kResidentBytes = 64ll << 20;
+template <int TBM = BM>
+__device__ __forceinline__ bool decode_tile(int t, const int* pref, int E, int NT, int K, int& e,
+                                            int& m, int& n) {
   e = find_expert(pref, E, t / NT);
   const int local = t - pref[e] * NT;
   const int mt = pref[e + 1] - pref[e];
-  const int grp = local / (GM * NT);
-  const int gm = min(GM, mt - grp * GM);
-  const int r = local - grp * GM * NT;
-  n = r / gm;
-  m = grp * GM + r % gm;
+  const long long rows_fit = kResidentBytes / ((long long)K * 2);
+  if ((long long)mt * TBM <= (long long)NT * BN) {
+    const int g = (int)max(1ll, min((long long)mt, rows_fit / TBM));
+    const int grp = local / (g * NT);
+    const int gm = min(g, mt - grp * g);
+    const int r = local - grp * g * NT;
+    n = r / gm;
+    m = grp * g + r % gm;
+    return true;
+  }
+  const int g = (int)max(1ll, min((long long)NT, rows_fit / BN));
+  const int grp = local / (g * mt);
+  const int gn = min(g, NT - grp * g);
+  const int r = local - grp * g * mt;
+  m = r / gn;
+  n = grp * g + r % gn;
+  return false;
 }
 
 template <bool BF16>
@@ -249,9 +287,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, armed = 0;
       uint32_t phase = 0;
       bool stop = false;
+#ifndef MOE_TC_HINTS
+#define MOE_TC_HINTS 1
+#endif
+      // The resident operand is marked evict_last.  The other one is NOT marked evict_first:
+      // each of its tiles is still read by every CTA of the same m-row / n-column, shortly apart.
+      const uint64_t keep = policy_evict_last(),
+                     other = MOE_TC_HINTS == 2 ? policy_evict_first() : policy_evict_normal();
       for (int t = blockIdx.x; t < total && !stop; t += gridDim.x) {
         int e, m, n;
-        decode_tile(t, pref, p.E, p.NT, e, m, n);
+        const bool a_res = decode_tile(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
+        uint64_t pa = a_res ? keep : other, pb = a_res ? other : keep;
+        if (MOE_TC_HINTS == 0) pa = pb = policy_evict_normal();
         const int a_row = __ldg(p.offsets + e) + m * BM;
         const int b_row = e * p.b_rows + n * (GATEUP ? BN / 2 : BN);
         for (int kb = 0; kb < p.KB; ++kb) {
@@ -261,12 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
           mbar_expect_tx(full_bar(stage), STAGE_BYTES);
-          tma_load_2d(sa, &mapA, full_bar(stage), kb * BK, a_row);
+          tma_load_2d(sa, &mapA, full_bar(stage), kb * BK, a_row, pa);
           if (GATEUP) {
-            tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, b_row);
-            tma_load_2d(sb + B_BYTES / 2, &mapB1, full_bar(stage), kb * BK, b_row);
+            tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, b_row, pb);
+            tma_load_2d(sb + B_BYTES / 2, &mapB1, full_bar(stage), kb * BK, b_row, pb);
           } else {
-            tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, b_row);
+            tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, b_row, pb);
           }
           ++armed;
           if (++stage == STAGES) {
@@ -330,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       int e, m, n;
-      decode_tile(t, pref, p.E, p.NT, e, m, n);
+      decode_tile(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
       const bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_f, p.status);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
@@ -405,6 +452,303 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ================================================================ CTA-pair kernels
+// A cluster of two CTAs on neighbouring SMs computes one 256 x 256 tile with cta_group::2 MMAs:
+// CTA r loads rows [128 r, 128 r + 128) of the tile's A rows and the r-th 128-row half of its B
+// rows (gate/up: r = 0 gate, r = 1 up; down: the two halves of the 256 output columns).  One
+// thread of CTA 0 issues tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16); the MMA reads both
+// CTAs' shared memory at the same offsets and leaves each CTA's 128 accumulator rows in that
+// CTA's TMEM.  With half of B per CTA a stage is 32 KB, so six stages fit, and each CTA pulls a
+// third fewer bytes per FLOP through L2 than a single-CTA 128 x 256 tile.
+// Synchronisation: both CTAs' TMA loads signal CTA 0's full barrier (CTA 0 arms it for both);
+// CTA 0's MMA commits are multicast to the empty / tmem-full barriers of both CTAs; all eight
+// epilogue warps arrive on CTA 0's tmem-empty barrier.  Waits are bounded as in the CTA kernel.
+constexpr int BM2 = 256, STAGES2 = 6;
+constexpr int A2_BYTES = 128 * BK * 2;  // 16 KB
+constexpr int B2_BYTES = 128 * BK * 2;  // 16 KB: half of the 256-row B tile
+constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;
+constexpr size_t kSmem2Bytes = 1024 + (size_t)STAGES2 * STAGE2_BYTES + 256 +
+                               (kMaxExperts + 4) * sizeof(int);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t ncluster_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t slot, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+               "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols)
+               : "memory");
+}
+// Arrives on `bar` (same offset) in every CTA of `mask` once all MMAs issued so far complete.
+__device__ __forceinline__ void umma_commit2(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void umma2_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// TMA load whose completion is signalled on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m,
+                                                 uint32_t cluster_bar, int x, int y,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(cluster_bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+template <bool GATEUP, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_experts_tc2(const __grid_constant__ CUtensorMap mapA,
+                    const __grid_constant__ CUtensorMap mapB0,
+                    const __grid_constant__ CUtensorMap mapB1, const TcParams p) {
+  extern __shared__ uint8_t tc_smem_raw[];
+  const uint32_t raw = smem_u32(tc_smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = tc_smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES2 * STAGE2_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES2 + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES2 + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES2 + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES2 + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 5);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* pref = reinterpret_cast<int*>(tmem_slot + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = (int)cluster_id_x(), npairs = (int)ncluster_x();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES2; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 8);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_f = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc2(smem_u32(tmem_slot), kTmemCols);
+  if (warp == 2) build_mtile_prefix(p.offsets, p.E, BM2, pref, lane);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&mapA);
+    tma_prefetch(&mapB0);
+    if (GATEUP) tma_prefetch(&mapB1);
+  }
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs: barriers initialised, TMEM allocated, prefix built
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = pref[p.E] * p.NT;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer (both CTAs)
+      int stage = 0, armed = 0;
+      uint32_t phase = 0;
+      bool stop = false;
+      const uint64_t keep = policy_evict_last(), other = policy_evict_normal();
+      const CUtensorMap* mapB = (GATEUP && !leader) ? &mapB1 : &mapB0;
+      for (int t = pair; t < total && !stop; t += npairs) {
+        int e, m, n;
+        const bool a_res = decode_tile<BM2>(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
+        const uint64_t pa = a_res ? keep : other, pb = a_res ? other : keep;
+        const int a_row = __ldg(p.offsets + e) + m * BM2 + (int)rank * 128;
+        const int b_row = GATEUP ? e * p.b_rows + n * (BN / 2)
+                                 : e * p.b_rows + n * BN + (int)rank * 128;
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_f, p.status)) {
+            stop = true;
+            break;
+          }
+          const uint32_t sa = base + stage * STAGE2_BYTES, sb = sa + A2_BYTES;
+          const uint32_t fb = map_to_rank(full_bar(stage), 0);
+          if (leader) mbar_expect_tx(full_bar(stage), 2 * STAGE2_BYTES);
+          tma_load_2d_pair(sa, &mapA, fb, kb * BK, a_row, pa);
+          tma_load_2d_pair(sb, mapB, fb, kb * BK, b_row, pb);
+          ++armed;
+          if (++stage == STAGES2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort_f && leader) {  // let copies still in flight land before the pair exits
+        for (int i = 0; i < min(armed, STAGES2); ++i) {
+          if (stage == 0) {
+            stage = STAGES2 - 1;
+            phase ^= 1u;
+          } else {
+            --stage;
+          }
+          wait_drain(full_bar(stage), phase);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (leader && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer (CTA 0 only)
+      constexpr uint32_t idesc = make_idesc(BF16, BM2, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool stop = false;
+      for (int t = pair; t < total && !stop; t += npairs) {
+        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_f, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < p.KB; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, abort_f, p.status)) {
+            stop = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + stage * STAGE2_BYTES, sb = sa + A2_BYTES;
+          const uint64_t da = make_sdesc(sa), db = make_sdesc(sb);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma2_f16(d_tmem, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
+          umma_commit2(empty_bar(stage), 0x3);
+          if (++stage == STAGES2) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (stop) break;
+        umma_commit2(tfull_bar(acc), 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      umma_commit2(drain_bar, 0x1);  // arrives once every MMA issued above has completed
+      wait_drain(drain_bar, 0);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (warps 2..5, both)
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = pair; t < total; t += npairs) {
+      int e, m, n;
+      decode_tile<BM2>(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
+      const bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_f, p.status);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      const int row = __ldg(p.offsets + e) + m * BM2 + (int)rank * 128 + q * 32 + lane;
+      const bool valid = row < __ldg(p.offsets + e + 1);
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      uint8_t* orow = p.out + (size_t)row * p.N * 2;
+      if (GATEUP) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + c * 32, g);
+          tmem_ld32(taddr + BN / 2 + c * 32, u);
+          tmem_wait_ld();
+          const int col0 = n * (BN / 2) + c * 32;
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (col0 + v * 8 < p.N) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  float a2[2];
+#pragma unroll
+                  for (int h = 0; h < 2; ++h) {
+                    const float gv = __uint_as_float(g[v * 8 + i * 2 + h]);
+                    const float uv = __uint_as_float(u[v * 8 + i * 2 + h]);
+                    a2[h] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                  }
+                  pk[i] = pack2<BF16>(a2[0], a2[1]);
+                }
+                st_v4(orow + (size_t)(col0 + v * 8) * 2, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+              }
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c * 32, r);
+          tmem_wait_ld();
+          const int col0 = n * BN + c * 32;
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (col0 + v * 8 < p.N) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  pk[i] = pack2<BF16>(__uint_as_float(r[v * 8 + i * 2]),
+                                      __uint_as_float(r[v * 8 + i * 2 + 1]));
+                st_v4(orow + (size_t)(col0 + v * 8) * 2, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_rank(tempty_bar(acc), 0));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncwarp();
+  cluster_sync_all();  // no CTA leaves while its pair may still signal it
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc2(tmem_base, kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -451,6 +795,41 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
   return cudaGetLastError();
 }
 
+template <bool GATEUP, bool BF16>
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                        const TcParams& p, int64_t rows, int dev, cudaStream_t s) {
+  auto kern = moe_experts_tc2<GATEUP, BF16>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmem2Bytes);
+  if (err != cudaSuccess) return err;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem2Bytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2);
+  // co-resident pairs on this device (queried once per device)
+  static int max_pairs[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_pairs[dev] == 0) {
+    int n = 0;
+    err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (err != cudaSuccess) return err;
+    if (n < 1) return cudaErrorLaunchOutOfResources;
+    max_pairs[dev] = n;
+  }
+  const int64_t upper = ((rows + BM2 - 1) / BM2 + p.E) * (int64_t)p.NT;  // >= number of tiles
+  const int pairs = (int)(upper < max_pairs[dev] ? upper : max_pairs[dev]);
+  cfg.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, p);
+}
+
 template <bool BF16>
 cudaError_t launch_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, const void* gate,
                         const void* up, const void* down, int E, int H, int I, void* y, void* a,
@@ -461,18 +840,23 @@ cudaError_t launch_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, c
   err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
 
+  // CTA pairs (256-row tiles) when experts average at least 128 rows; below that the pair's
+  // taller tiles mostly multiply padding and single CTAs stream the weights as well.
+  const bool pair = rows >= (int64_t)128 * E;
   CUtensorMap mx, mg, mu, ma, md;
   if (!make_map(&mx, x_d, BF16, H, rows, BM) || !make_map(&mg, gate, BF16, H, (int64_t)E * I, BN / 2) ||
       !make_map(&mu, up, BF16, H, (int64_t)E * I, BN / 2) || !make_map(&ma, a, BF16, I, rows, BM) ||
-      !make_map(&md, down, BF16, I, (int64_t)E * H, BN))
+      !make_map(&md, down, BF16, I, (int64_t)E * H, pair ? BN / 2 : BN))
     return cudaErrorInvalidValue;
 
   TcParams p1{offsets, (uint8_t*)a, status, E, I, (H + BK - 1) / BK, (I + BN / 2 - 1) / (BN / 2), I};
-  err = launch_one<true, BF16>(mx, mg, mu, p1, rows, sms, s);
+  err = pair ? launch_pair<true, BF16>(mx, mg, mu, p1, rows, dev, s)
+             : launch_one<true, BF16>(mx, mg, mu, p1, rows, sms, s);
   if (err != cudaSuccess) return err;
   if (between && (err = cudaEventRecord(between, s)) != cudaSuccess) return err;
   TcParams p2{offsets, (uint8_t*)y, status, E, H, (I + BK - 1) / BK, (H + BN - 1) / BN, H};
-  return launch_one<false, BF16>(ma, md, md, p2, rows, sms, s);
+  return pair ? launch_pair<false, BF16>(ma, md, md, p2, rows, dev, s)
+              : launch_one<false, BF16>(ma, md, md, p2, rows, sms, s);
 }
 
 }  // namespace
