@@ -44,7 +44,8 @@ typedef enum {
   MOE_ERR_WORKSPACE = 5, /* ws is NULL, misaligned or smaller than the query result       */
   MOE_ERR_CUDA = 6,      /* CUDA runtime / launch error                                   */
   MOE_ERR_TIMEOUT = 7,   /* (device status only) a pipeline wait exceeded its time limit  */
-  MOE_ERR_INDEX = 8      /* (device status only) an expert index >= E reached dispatch    */
+  MOE_ERR_INDEX = 8,     /* (device status only) an expert index >= E reached dispatch    */
+  MOE_ERR_ARG = 9        /* a scalar argument is out of range (e.g. scale not finite > 0)  */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_F16 = 1, MOE_BF16 = 2 } moe_dtype;
@@ -71,6 +72,27 @@ int moe_abi_version(void);
  */
 int moe_route(const void* logits, int ldt, int64_t T, int64_t E, int top_k, int renormalize,
               uint32_t* idx, void* w, moe_stream_t stream);
+
+/*
+ * moe_route_sigmoid_grouped — route_sigmoid_grouped(logits, bias, GroupRoutingOptions) of §10
+ * "Gruppenbeschränktes Sigmoid-MoE-Routing".
+ *
+ * s = sigmoid(logit); c = s + bias[e] (bias: FP32 [E] device pointer, or NULL for none; it changes
+ * the selection only).  The E experts form `groups` contiguous groups of E / groups; a group's
+ * score is its largest c, or with group_top_two != 0 the sum of its two largest c.  The
+ * `selected_groups` best groups are kept (ties: lower group id), then the top_k experts inside
+ * them by c (ties: lower id); idx lists them in that order.  w = s of the chosen experts,
+ * divided by their sum if renormalize != 0, times `scale`, rounded to `ldt`.  The selection is
+ * decided in float64.  Rows whose corrected scores hold a NaN get NaN weights and ids 0..k-1.
+ * Limits (as §10 states): 1 <= E <= 1024, 1 <= groups <= 128, E % groups == 0,
+ * 1 <= selected_groups <= groups, 1 <= top_k <= 64, top_k <= selected_groups * E / groups,
+ * E / groups >= 2 with group_top_two (else MOE_ERR_SHAPE); scale finite and > 0 (else MOE_ERR_ARG).
+ * logits [T, E] dtype ldt; idx [T, top_k] uint32; w [T, top_k] dtype ldt.
+ */
+int moe_route_sigmoid_grouped(const void* logits, int ldt, const float* bias, int64_t T,
+                              int64_t E, int top_k, int groups, int selected_groups,
+                              int group_top_two, int renormalize, float scale, uint32_t* idx,
+                              void* w, moe_stream_t stream);
 
 /*
  * moe_dispatch — RoutingPlan::dispatch(input) of §3/§5 "Expertengewichte und Verteilung".
@@ -164,6 +186,18 @@ size_t moe_forward_workspace_bytes(int64_t T, int64_t E, int64_t H, int64_t I, i
 int moe_forward(const void* x, const void* logits, int ldt, const void* gate, const void* up,
                 const void* down, int wdt, int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
                 int renormalize, void* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_forward_sigmoid_grouped — SwiGluExperts::forward_sigmoid_grouped of §10: group-limited
+ * sigmoid routing (as moe_route_sigmoid_grouped), then dispatch, experts and combine exactly as
+ * moe_forward.  Workspace: moe_forward_workspace_bytes(T, E, H, I, top_k, ldt, wdt).
+ */
+int moe_forward_sigmoid_grouped(const void* x, const void* logits, int ldt, const float* bias,
+                                const void* gate, const void* up, const void* down, int wdt,
+                                int64_t T, int64_t E, int64_t H, int64_t I, int top_k, int groups,
+                                int selected_groups, int group_top_two, int renormalize,
+                                float scale, void* out, void* ws, size_t ws_bytes,
+                                moe_stream_t stream);
 
 /*
  * moe_forward_with_events — moe_forward that also records caller-created CUDA events

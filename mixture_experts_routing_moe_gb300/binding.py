@@ -21,13 +21,16 @@ MOE_F32, MOE_F16, MOE_BF16 = 0, 1, 2
 DTYPE_CODE = {torch.float32: MOE_F32, torch.float16: MOE_F16, torch.bfloat16: MOE_BF16}
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_NULL", 2: "MOE_ERR_SHAPE", 3: "MOE_ERR_DTYPE",
           4: "MOE_ERR_ALIGN", 5: "MOE_ERR_WORKSPACE", 6: "MOE_ERR_CUDA", 7: "MOE_ERR_TIMEOUT",
-          8: "MOE_ERR_INDEX"}
+          8: "MOE_ERR_INDEX", 9: "MOE_ERR_ARG"}
 
 _i64, _int, _sz, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+_f32 = ctypes.c_float
 _SIGS = {
     "moe_abi_version": (_int, []),
     "moe_status_string": (ctypes.c_char_p, [_int]),
     "moe_route": (_int, [_vp, _int, _i64, _i64, _int, _int, _vp, _vp, _vp]),
+    "moe_route_sigmoid_grouped": (_int, [_vp, _int, _vp, _i64, _i64, _int, _int, _int, _int, _int,
+                                         _f32, _vp, _vp, _vp]),
     "moe_dispatch_workspace_bytes": (_sz, [_i64, _i64, _int]),
     "moe_dispatch": (_int, [_vp, _int, _i64, _i64, _vp, _i64, _int, _vp, _vp, _vp, _vp, _vp, _sz,
                             _vp]),
@@ -40,6 +43,9 @@ _SIGS = {
     "moe_forward_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _int, _int, _int]),
     "moe_forward": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _int, _i64, _i64, _i64, _i64, _int, _int,
                            _vp, _vp, _sz, _vp]),
+    "moe_forward_sigmoid_grouped": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _vp, _int, _i64, _i64,
+                                           _i64, _i64, _int, _int, _int, _int, _int, _f32, _vp,
+                                           _vp, _sz, _vp]),
     "moe_forward_with_events": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _int, _i64, _i64, _i64,
                                        _i64, _int, _int, _vp, _vp, _sz, _vp, _vp]),
     "moe_device_status": (_int, [_vp, _sz, _vp]),
@@ -116,6 +122,26 @@ def moe_route(logits, top_k: int, renormalize: bool = True, idx=None, w=None, st
     _cuda(idx, w)
     _check(lib().moe_route(_ptr(logits), _code(logits), T, E, top_k, int(bool(renormalize)),
                            _ptr(idx), _ptr(w), _stream(stream)), "moe_route")
+    return idx, w
+
+
+def moe_route_sigmoid_grouped(logits, top_k: int, groups: int, selected_groups: int,
+                              group_top_two: bool = True, renormalize: bool = True,
+                              scale: float = 1.0, bias=None, idx=None, w=None, stream=None):
+    """route_sigmoid_grouped(logits, bias, GroupRoutingOptions) -> (idx uint32 [T,k], w [T,k])."""
+    _cuda(logits, bias)
+    if bias is not None and bias.dtype != torch.float32:
+        raise MoeError(3, "bias must be float32")
+    T, E = logits.shape
+    if idx is None:
+        idx = torch.empty(T, top_k, dtype=torch.uint32, device=logits.device)
+    if w is None:
+        w = torch.empty(T, top_k, dtype=logits.dtype, device=logits.device)
+    _cuda(idx, w)
+    _check(lib().moe_route_sigmoid_grouped(
+        _ptr(logits), _code(logits), _ptr(bias), T, E, top_k, groups, selected_groups,
+        int(bool(group_top_two)), int(bool(renormalize)), float(scale), _ptr(idx), _ptr(w),
+        _stream(stream)), "moe_route_sigmoid_grouped")
     return idx, w
 
 
@@ -198,6 +224,27 @@ def moe_forward(x, logits, gate, up, down, top_k: int, renormalize: bool = True,
     _check(lib().moe_forward(_ptr(x), _ptr(logits), _code(logits), _ptr(gate), _ptr(up),
                              _ptr(down), _code(gate), T, E, H, I, top_k, int(bool(renormalize)),
                              _ptr(out), _ptr(ws), ws.numel(), _stream(stream)), "moe_forward")
+    return out
+
+
+def moe_forward_sigmoid_grouped(x, logits, gate, up, down, top_k: int, groups: int,
+                                selected_groups: int, group_top_two: bool = True,
+                                renormalize: bool = True, scale: float = 1.0, bias=None, out=None,
+                                ws=None, stream=None):
+    """SwiGluExperts::forward_sigmoid_grouped -> out [T, H]."""
+    _cuda(x, logits, gate, up, down, bias)
+    T, H = x.shape
+    E, I, _ = gate.shape
+    out = torch.empty_like(x) if out is None else out
+    if ws is None:
+        ws = torch.empty(max(forward_workspace_bytes(T, E, H, I, top_k, logits.dtype, x.dtype), 256),
+                         dtype=torch.uint8, device=x.device)
+    _cuda(out, ws)
+    _check(lib().moe_forward_sigmoid_grouped(
+        _ptr(x), _ptr(logits), _code(logits), _ptr(bias), _ptr(gate), _ptr(up), _ptr(down),
+        _code(gate), T, E, H, I, top_k, groups, selected_groups, int(bool(group_top_two)),
+        int(bool(renormalize)), float(scale), _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+        "moe_forward_sigmoid_grouped")
     return out
 
 

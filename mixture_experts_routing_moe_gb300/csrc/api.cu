@@ -1,6 +1,7 @@
 // C-ABI entry points of libmoe (declared in include/moe.h): host-side validation, workspace
 // layout and the launch sequence.  No entry point allocates, frees or synchronises, except
 // moe_device_status, whose job is to read the device status word back.
+#include <math.h>
 #include <string.h>
 
 #include "common.cuh"
@@ -78,9 +79,79 @@ int run_experts(const void* x_d, const int32_t* offsets, int64_t rows, const voi
                                        (int)I, y, a, status, s, between));
 }
 
+int check_sigmoid_args(int64_t T, int64_t E, int top_k, int G, int SG, int top_two, float scale) {
+  if (T < 0 || E < 1 || E > kMaxE || G < 1 || G > 128 || E % G != 0) return MOE_ERR_SHAPE;
+  if (SG < 1 || SG > G || top_k < 1 || top_k > 64) return MOE_ERR_SHAPE;
+  if ((int64_t)top_k > (int64_t)SG * (E / G)) return MOE_ERR_SHAPE;
+  if (top_two && E / G < 2) return MOE_ERR_SHAPE;
+  if (T * top_k >= kMaxRows) return MOE_ERR_SHAPE;
+  if (!(scale > 0.f) || !isfinite(scale)) return MOE_ERR_ARG;
+  return MOE_OK;
+}
+
+// How a forward routes its tokens: the softmax router of §4 or the sigmoid router of §10.
+struct RouteSpec {
+  bool sigmoid;
+  int renormalize;
+  const float* bias;
+  int groups, selected_groups, top_two;
+  float scale;
+};
+
 // Records events[i] on s when an event array is given.
 bool record(void* const* events, int i, cudaStream_t s) {
   return !events || cudaEventRecord((cudaEvent_t)events[i], s) == cudaSuccess;
+}
+
+// The fused forward: route (softmax or sigmoid), dispatch, experts, combine on one stream.
+int run_forward(const void* x, const void* logits, int ldt, const void* gate, const void* up,
+                const void* down, int wdt, int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
+                const RouteSpec& rs, void* out, void* ws, size_t ws_bytes, cudaStream_t s,
+                void* const* events) {
+  if (!valid_dtype(ldt) || !valid_dtype(wdt)) return MOE_ERR_DTYPE;
+  int st = check_experts_shape(T * top_k, E, H, I);
+  if (st != MOE_OK) return st;
+  if (!gate || !up || !down) return MOE_ERR_NULL;
+  if (T == 0) return MOE_OK;
+  if (!x || !logits || !out) return MOE_ERR_NULL;
+  if (!aligned16(x) || (H * (int64_t)dtype_size(wdt)) % 16 != 0) return MOE_ERR_ALIGN;
+  if (wdt != MOE_F32) {
+    const void* ptrs[5] = {x, gate, up, down, out};
+    st = check_tc_align(H, I, ptrs, 5);
+    if (st != MOE_OK) return st;
+  }
+  const FwdLayout L = fwd_layout(T, E, H, I, top_k, ldt, wdt);
+  if (!ws || ((uintptr_t)ws & 255u) != 0 || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+
+  uint8_t* b = (uint8_t*)ws;
+  unsigned* status = (unsigned*)ws;
+  uint32_t* idx = (uint32_t*)(b + L.idx);
+  void* w = b + L.w;
+  uint32_t* ros = (uint32_t*)(b + L.ros);
+  uint32_t* tor = (uint32_t*)(b + L.tor);
+  int32_t* offsets = (int32_t*)(b + L.offsets);
+  int32_t* hist = (int32_t*)(b + L.hist);
+  void* xd = b + L.xd;
+  void* a = b + L.a;
+  const int64_t R = T * top_k;
+
+  if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!record(events, 0, s)) return MOE_ERR_CUDA;
+  cudaError_t err =
+      rs.sigmoid
+          ? launch_route_sigmoid(logits, ldt, rs.bias, T, (int)E, top_k, rs.groups,
+                                 rs.selected_groups, rs.top_two != 0, rs.renormalize != 0,
+                                 rs.scale, idx, w, s)
+          : launch_route(logits, ldt, T, (int)E, top_k, rs.renormalize != 0, idx, w, s);
+  if (err != cudaSuccess || !record(events, 1, s)) return MOE_ERR_CUDA;
+  err = launch_dispatch(x, wdt, T, H, idx, (int)E, top_k, xd, offsets, tor, ros, hist, status, s);
+  if (err != cudaSuccess || !record(events, 2, s)) return MOE_ERR_CUDA;
+  st = run_experts(xd, offsets, R, gate, up, down, wdt, E, H, I, /*y=*/xd, a, status, s,
+                   events ? (cudaEvent_t)events[3] : nullptr);
+  if (st != MOE_OK || !record(events, 4, s)) return st != MOE_OK ? st : MOE_ERR_CUDA;
+  err = launch_combine(xd, wdt, ros, w, ldt, T, H, top_k, out, s);
+  if (err != cudaSuccess || !record(events, 5, s)) return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 }  // namespace
@@ -100,6 +171,7 @@ const char* moe_status_string(int st) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_TIMEOUT: return "a device pipeline wait timed out";
     case MOE_ERR_INDEX: return "an expert index >= E reached dispatch";
+    case MOE_ERR_ARG: return "a scalar argument is out of range";
   }
   return "unknown status";
 }
@@ -113,6 +185,20 @@ int moe_route(const void* logits, int ldt, int64_t T, int64_t E, int top_k, int 
   if (!logits || !idx || !w) return MOE_ERR_NULL;
   return cuda_status(launch_route(logits, ldt, T, (int)E, top_k, renormalize != 0, idx, w,
                                   (cudaStream_t)stream));
+}
+
+int moe_route_sigmoid_grouped(const void* logits, int ldt, const float* bias, int64_t T,
+                              int64_t E, int top_k, int groups, int selected_groups,
+                              int group_top_two, int renormalize, float scale, uint32_t* idx,
+                              void* w, moe_stream_t stream) {
+  if (!valid_dtype(ldt)) return MOE_ERR_DTYPE;
+  const int st = check_sigmoid_args(T, E, top_k, groups, selected_groups, group_top_two, scale);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!logits || !idx || !w) return MOE_ERR_NULL;
+  return cuda_status(launch_route_sigmoid(logits, ldt, bias, T, (int)E, top_k, groups,
+                                          selected_groups, group_top_two != 0, renormalize != 0,
+                                          scale, idx, w, (cudaStream_t)stream));
 }
 
 size_t moe_dispatch_workspace_bytes(int64_t T, int64_t E, int top_k) {
@@ -223,48 +309,25 @@ int moe_forward_with_events(const void* x, const void* logits, int ldt, const vo
                             const void* up, const void* down, int wdt, int64_t T, int64_t E,
                             int64_t H, int64_t I, int top_k, int renormalize, void* out, void* ws,
                             size_t ws_bytes, moe_stream_t stream, void* const* events) {
-  if (!valid_dtype(ldt) || !valid_dtype(wdt)) return MOE_ERR_DTYPE;
-  int st = check_route_shape(T, E, top_k);
+  const int st = check_route_shape(T, E, top_k);
   if (st != MOE_OK) return st;
-  st = check_experts_shape(T * top_k, E, H, I);
+  const RouteSpec r{false, renormalize, nullptr, 1, 1, 0, 1.f};
+  return run_forward(x, logits, ldt, gate, up, down, wdt, T, E, H, I, top_k, r, out, ws, ws_bytes,
+                     (cudaStream_t)stream, events);
+}
+
+int moe_forward_sigmoid_grouped(const void* x, const void* logits, int ldt, const float* bias,
+                                const void* gate, const void* up, const void* down, int wdt,
+                                int64_t T, int64_t E, int64_t H, int64_t I, int top_k, int groups,
+                                int selected_groups, int group_top_two, int renormalize,
+                                float scale, void* out, void* ws, size_t ws_bytes,
+                                moe_stream_t stream) {
+  if (!valid_dtype(ldt)) return MOE_ERR_DTYPE;
+  const int st = check_sigmoid_args(T, E, top_k, groups, selected_groups, group_top_two, scale);
   if (st != MOE_OK) return st;
-  if (!gate || !up || !down) return MOE_ERR_NULL;
-  if (T == 0) return MOE_OK;
-  if (!x || !logits || !out) return MOE_ERR_NULL;
-  if (!aligned16(x) || (H * (int64_t)dtype_size(wdt)) % 16 != 0) return MOE_ERR_ALIGN;
-  if (wdt != MOE_F32) {
-    const void* ptrs[5] = {x, gate, up, down, out};
-    st = check_tc_align(H, I, ptrs, 5);
-    if (st != MOE_OK) return st;
-  }
-  const FwdLayout L = fwd_layout(T, E, H, I, top_k, ldt, wdt);
-  if (!ws || ((uintptr_t)ws & 255u) != 0 || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-
-  cudaStream_t s = (cudaStream_t)stream;
-  uint8_t* b = (uint8_t*)ws;
-  unsigned* status = (unsigned*)ws;
-  uint32_t* idx = (uint32_t*)(b + L.idx);
-  void* w = b + L.w;
-  uint32_t* ros = (uint32_t*)(b + L.ros);
-  uint32_t* tor = (uint32_t*)(b + L.tor);
-  int32_t* offsets = (int32_t*)(b + L.offsets);
-  int32_t* hist = (int32_t*)(b + L.hist);
-  void* xd = b + L.xd;
-  void* a = b + L.a;
-  const int64_t R = T * top_k;
-
-  if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (!record(events, 0, s)) return MOE_ERR_CUDA;
-  cudaError_t err = launch_route(logits, ldt, T, (int)E, top_k, renormalize != 0, idx, w, s);
-  if (err != cudaSuccess || !record(events, 1, s)) return MOE_ERR_CUDA;
-  err = launch_dispatch(x, wdt, T, H, idx, (int)E, top_k, xd, offsets, tor, ros, hist, status, s);
-  if (err != cudaSuccess || !record(events, 2, s)) return MOE_ERR_CUDA;
-  st = run_experts(xd, offsets, R, gate, up, down, wdt, E, H, I, /*y=*/xd, a, status, s,
-                   events ? (cudaEvent_t)events[3] : nullptr);
-  if (st != MOE_OK || !record(events, 4, s)) return st != MOE_OK ? st : MOE_ERR_CUDA;
-  err = launch_combine(xd, wdt, ros, w, ldt, T, H, top_k, out, s);
-  if (err != cudaSuccess || !record(events, 5, s)) return MOE_ERR_CUDA;
-  return MOE_OK;
+  const RouteSpec r{true, renormalize, bias, groups, selected_groups, group_top_two, scale};
+  return run_forward(x, logits, ldt, gate, up, down, wdt, T, E, H, I, top_k, r, out, ws, ws_bytes,
+                     (cudaStream_t)stream, nullptr);
 }
 
 int moe_device_status(void* ws, size_t ws_bytes, moe_stream_t stream) {

@@ -17,6 +17,11 @@ constexpr unsigned kStatusIndex = 2u;
 cudaError_t launch_route(const void* logits, int ldt, int64_t T, int E, int k, int renorm,
                          uint32_t* idx, void* w, cudaStream_t s);
 
+// Group-limited sigmoid routing (float64 selection); bias may be null.
+cudaError_t launch_route_sigmoid(const void* logits, int ldt, const float* bias, int64_t T, int E,
+                                 int k, int G, int SG, int top_two, int renorm, float scale,
+                                 uint32_t* idx, void* w, cudaStream_t s);
+
 // Dispatch splits the R = T*k slots into W contiguous chunks of CH slots, one per warp.
 struct DispatchPlan {
   int W;   // chunks (warps)

@@ -142,6 +142,158 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// Fast path for 16-bit logits with E <= 64 (E % 8 == 0, 16-byte aligned rows) and top_k <= 8:
+// one row per thread.  Keys are 32-bit: monotone 16-bit value bits << 16 | (0xFFFF - id), so a
+// larger key is a larger logit and equal logits prefer the lower id.  Each 16-byte vector (8
+// experts) is sorted by an 8-input sorting network and merged into the running sorted top 8 with
+// a bitonic merge (elementwise max against the reversed list, then a half-cleaner).  The softmax
+// denominator is accumulated online over the vectors (rescaled when the running max grows);
+// with renormalisation only the selected experts' exponentials are needed.
+__device__ __forceinline__ void ce_desc(uint32_t& a, uint32_t& b) {
+  const uint32_t hi = max(a, b), lo = min(a, b);
+  a = hi;
+  b = lo;
+}
+__device__ __forceinline__ void sort8_desc(uint32_t (&k)[8]) {
+  ce_desc(k[0], k[1]); ce_desc(k[2], k[3]); ce_desc(k[4], k[5]); ce_desc(k[6], k[7]);
+  ce_desc(k[0], k[2]); ce_desc(k[1], k[3]); ce_desc(k[4], k[6]); ce_desc(k[5], k[7]);
+  ce_desc(k[1], k[2]); ce_desc(k[5], k[6]);
+  ce_desc(k[0], k[4]); ce_desc(k[1], k[5]); ce_desc(k[2], k[6]); ce_desc(k[3], k[7]);
+  ce_desc(k[2], k[4]); ce_desc(k[3], k[5]);
+  ce_desc(k[1], k[2]); ce_desc(k[3], k[4]); ce_desc(k[5], k[6]);
+}
+// top: sorted descending; g: sorted descending.  Leaves the 8 largest of both in `top`, sorted.
+__device__ __forceinline__ void merge_top8(uint32_t (&top)[8], const uint32_t (&g)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) top[i] = max(top[i], g[7 - i]);  // bitonic, holds the top 8
+  ce_desc(top[0], top[4]); ce_desc(top[1], top[5]); ce_desc(top[2], top[6]); ce_desc(top[3], top[7]);
+  ce_desc(top[0], top[2]); ce_desc(top[1], top[3]); ce_desc(top[4], top[6]); ce_desc(top[5], top[7]);
+  ce_desc(top[0], top[1]); ce_desc(top[2], top[3]); ce_desc(top[4], top[5]); ce_desc(top[6], top[7]);
+}
+template <typename T>
+__device__ __forceinline__ float bits16_to_float(uint32_t b) {
+  if constexpr (sizeof(T) == 2 && Dt<T>::code == MOE_BF16) {
+    return __uint_as_float(b << 16);
+  } else {
+    return __half2float(__ushort_as_half((unsigned short)b));
+  }
+}
+
+template <typename T, int NV, bool RENORM>
+__global__ void __launch_bounds__(256)
+    moe_route16_small(const uint4* __restrict__ logits, int64_t T_, int k,
+                      uint32_t* __restrict__ idx_out, T* __restrict__ w_out) {
+  constexpr uint32_t EXPMASK = Dt<T>::code == MOE_BF16 ? 0x7F80u : 0x7C00u;
+  const int64_t row0 = (int64_t)blockIdx.x * 256;
+  const int64_t row = row0 + threadIdx.x;
+  // E = 64: the block's 256 rows (32 KB, contiguous) are read with coalesced 16-byte loads into
+  // shared memory, vector v of row r stored at slot v ^ (r & 7) so that the row-per-thread reads
+  // below hit 8 different bank groups per 8 lanes.
+  constexpr bool STAGED = NV == 8;
+  __shared__ uint4 tile[STAGED ? 256 * 8 : 1];
+  if (STAGED) {
+    const int64_t left = T_ - row0;
+    const int n = (int)((left < 256 ? left : 256) * 8);
+    const uint4* bsrc = logits + row0 * 8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int c = threadIdx.x + i * 256;
+      if (c < n) tile[(c & ~7) | ((c & 7) ^ ((c >> 3) & 7))] = ld_nc_v4(bsrc + c);
+    }
+    __syncthreads();
+  }
+  if (row >= T_) return;
+  const uint4* src = logits + row * NV;
+  uint32_t top[8];
+  uint32_t minv = 0xFFFFFFFFu;  // smallest monotone value (catches negative NaNs)
+  float m = -INFINITY, s = 0.f;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const uint4 q = STAGED ? tile[threadIdx.x * 8 + (v ^ (threadIdx.x & 7))] : ld_nc_v4(src + v);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    uint32_t g[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // monotone map of both 16-bit halves: negative -> all bits flipped, else sign bit set
+      const uint32_t t = w[i] ^ ((((w[i] >> 15) & 0x00010001u) * 0xFFFFu) | 0x80008000u);
+      minv = min(minv, min(t & 0xFFFFu, t >> 16));
+      const uint32_t e0 = v * 8 + i * 2;
+      g[2 * i] = (t << 16) | (0xFFFFu - e0);
+      g[2 * i + 1] = (t & 0xFFFF0000u) | (0xFFFFu - (e0 + 1));
+    }
+    if (!RENORM) {  // online softmax denominator
+      float x[8], gm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[2 * i] = bits16_to_float<T>(w[i] & 0xFFFFu);
+        x[2 * i + 1] = bits16_to_float<T>(w[i] >> 16);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) gm = fmaxf(gm, x[i]);
+      const float mn = fmaxf(m, gm);
+      const float ref = mn == -INFINITY ? 0.f : mn;  // all -inf so far: every term is 0
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc += __expf(x[i] - ref);
+      s = (m == -INFINITY ? 0.f : s * __expf(m - mn)) + acc;
+      m = mn;
+    }
+    sort8_desc(g);
+    if (v == 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) top[i] = g[i];
+    } else {
+      merge_top8(top, g);
+    }
+  }
+  // poisoned: largest value NaN / +inf / -inf (the last means every value is -inf), or a
+  // negative NaN at the bottom
+  const uint32_t tb = top[0] >> 16;
+  const uint32_t vb0 = (tb & 0x8000u) ? (tb & 0x7FFFu) : (~tb & 0xFFFFu);
+  const uint32_t vbm = (minv & 0x8000u) ? (minv & 0x7FFFu) : (~minv & 0xFFFFu);
+  const bool poisoned = (vb0 & 0x7FFFu) >= EXPMASK || ((vbm & 0x7FFFu) > EXPMASK);
+  const float x0 = bits16_to_float<T>(vb0);
+  float ex[8], sel = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t b = top[j] >> 16;
+    const uint32_t vb = (b & 0x8000u) ? (b & 0x7FFFu) : (~b & 0xFFFFu);
+    ex[j] = __expf(bits16_to_float<T>(vb) - x0);
+    if (j < k) sel += ex[j];
+  }
+  const float denom = RENORM ? sel : s * __expf(m - x0);
+  uint32_t* io = idx_out + row * k;
+  T* wo = w_out + row * k;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      io[j] = poisoned ? (uint32_t)j : 0xFFFFu - (top[j] & 0xFFFFu);
+      wo[j] = Dt<T>::from_f(poisoned ? __int_as_float(0x7FC00000) : ex[j] / denom);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_route16_small(const void* logits, int64_t T_, int E, int k, int renorm,
+                                 uint32_t* idx, void* w, cudaStream_t s) {
+  const unsigned blocks = (unsigned)((T_ + 255) / 256);
+  const uint4* l = (const uint4*)logits;
+#define MOE_R16(NV)                                                                             \
+  case NV:                                                                                      \
+    if (renorm)                                                                                 \
+      moe_route16_small<T, NV, true><<<blocks, 256, 0, s>>>(l, T_, k, idx, (T*)w);              \
+    else                                                                                        \
+      moe_route16_small<T, NV, false><<<blocks, 256, 0, s>>>(l, T_, k, idx, (T*)w);             \
+    break;
+  switch (E / 8) {
+    MOE_R16(1) MOE_R16(2) MOE_R16(3) MOE_R16(4) MOE_R16(5) MOE_R16(6) MOE_R16(7) MOE_R16(8)
+    default: return cudaErrorInvalidValue;
+  }
+#undef MOE_R16
+  return cudaGetLastError();
+}
+
 template <typename T, int L, int C>
 cudaError_t launch_route_lc(const void* logits, int64_t T_, int E, int k, int renorm,
                             uint32_t* idx, void* w, cudaStream_t s) {
@@ -171,6 +323,10 @@ template <typename T>
 cudaError_t launch_route_t(const void* logits, int64_t T_, int E, int k, int renorm, uint32_t* idx,
                            void* w, cudaStream_t s) {
   constexpr int VW = 16 / sizeof(T);
+  if constexpr (sizeof(T) == 2) {
+    if (E <= 64 && E % 8 == 0 && k <= 8 && ((uintptr_t)logits) % 16 == 0)
+      return launch_route16_small<T>(logits, T_, E, k, renorm, idx, w, s);
+  }
   // choose lanes-per-row L and elements-per-lane C (a multiple of the vector width) with L*C >= E
   if (E <= 1 * VW) return launch_route_lc<T, 1, VW>(logits, T_, E, k, renorm, idx, w, s);
   if (E <= 2 * VW) return launch_route_lc<T, 2, VW>(logits, T_, E, k, renorm, idx, w, s);

@@ -22,11 +22,11 @@ F32, F16, BF16 = B.MOE_F32, B.MOE_F16, B.MOE_BF16
 
 def test_exports_every_header_function(L):
     names = B.header_functions()
-    assert len(names) == 13
+    assert len(names) == 15
     for n in names:
         assert hasattr(L, n), n
     assert L.moe_abi_version() == 1
-    for code in range(9):
+    for code in range(10):
         assert L.moe_status_string(code) not in (None, b"unknown status")
 
 
@@ -118,3 +118,25 @@ def test_valid_call_without_gpu_fails_loudly(L):
     assert L.moe_route(FAKE, BF16, 16, 8, 2, 1, FAKE, FAKE, None) == 6
     with pytest.raises(Exception):
         B.moe_route(torch.zeros(4, 8), 2)
+
+
+def test_sigmoid_router_rejects(L):
+    def call(ldt=BF16, T=16, E=64, k=8, G=8, SG=4, top2=1, scale=1.0, logits=FAKE):
+        return L.moe_route_sigmoid_grouped(logits, ldt, None, T, E, k, G, SG, top2, 1, scale, FAKE,
+                                           FAKE, None)
+    assert call(ldt=5) == 3
+    assert call(G=7) == 2             # E % groups != 0
+    assert call(G=256, E=256) == 2    # more than 128 groups
+    assert call(SG=9) == 2            # selected_groups > groups
+    assert call(k=65, E=128) == 2     # top_k > 64
+    assert call(k=9, SG=1) == 2       # top_k > selected_groups * E / groups
+    assert call(G=64, top2=1) == 2    # group_top_two needs >= 2 experts per group
+    assert call(scale=0.0) == 9
+    assert call(scale=float("inf")) == 9
+    assert call(scale=float("nan")) == 9
+    assert call(logits=None) == 1
+    assert call(T=0, logits=None) == 0
+    need = L.moe_forward_workspace_bytes(16, 64, 128, 256, 8, BF16, BF16)
+    assert L.moe_forward_sigmoid_grouped(FAKE, FAKE, BF16, None, FAKE, FAKE, FAKE, BF16, 16, 64,
+                                         128, 256, 8, 8, 4, 1, 1, -1.0, FAKE, FAKE, need,
+                                         None) == 9
