@@ -44,6 +44,11 @@ values, optionally renormalised, times `scale`; ties prefer smaller ids.  Readin
   S3 rows whose corrected scores hold a NaN keep NaN weights and select ids 0..k-1;
   S4 weights are rounded once to the logits dtype after renormalisation and scaling.
 
+Router weights of a fixed selection and their gradient follow §12 "MoE-Training erster Ordnung":
+FP32 weights [T, k] for given indices (softmax over all experts, or sigmoid), optional
+renormalisation over the k slots, then `scale`; repeated indices gather; an invalid index makes
+the whole row NaN; the gradient is with respect to the logits of the continuous weights only.
+
 Pins (tests/test_oracle_pins.py) tie each function to something other than itself: closed forms,
 library routines (torch float64 softmax and silu, numpy's float32 cast), brute force on tiny
 inputs, and invariants.  Parity unpinned: R1 for two *different* logits whose FP32 softmax values
@@ -57,6 +62,7 @@ __all__ = [
     "DTYPES", "to_f64", "round_to_dtype", "encode", "poisoned_rows", "softmax", "select_topk",
     "route", "dispatch", "gather", "silu", "swiglu", "experts", "combine", "forward",
     "forward_rows", "sigmoid", "route_sigmoid_grouped", "forward_sigmoid_grouped",
+    "selected_router_weights", "selected_router_backward",
 ]
 
 DTYPES = ("f32", "f16", "bf16")
@@ -348,3 +354,77 @@ def forward_sigmoid_grouped(x, x_dtype, logits, logits_dtype, bias, gate, up, do
     out = combine(y, row_of_slot, w)
     return {"idx": idx, "w": w, "counts": counts, "offsets": offsets,
             "out_unrounded": out, "out": round_to_dtype(out, x_dtype)}
+
+
+# --------------------------------------------------------------------------------------------
+# router weights of a fixed selection and their backward (§12 "MoE-Training erster Ordnung")
+# --------------------------------------------------------------------------------------------
+def _selection_scores(logits, scoring):
+    if scoring == "softmax":
+        return softmax(logits)
+    if scoring == "sigmoid":
+        return sigmoid(logits)
+    raise ValueError(scoring)
+
+
+def selected_router_weights(logits: np.ndarray, idx: np.ndarray, scoring: str, renormalize: bool,
+                            scale: float) -> np.ndarray:
+    """w[t, j] = scale * p[t, idx[t, j]] (divided by sum_j p[t, idx[t, j]] when renormalising),
+    p = softmax over all experts or sigmoid.  Repeated indices gather the same p; a row with an
+    index outside [0, E) is all NaN.  float64 [T, k]; the page returns FP32."""
+    T, E = logits.shape
+    idx = np.asarray(idx).astype(np.int64)
+    bad = ((idx < 0) | (idx >= E)).any(axis=1)
+    p = _selection_scores(logits, scoring)
+    w = np.take_along_axis(p, np.where(idx < 0, 0, np.minimum(idx, E - 1)), axis=1)
+    if renormalize:
+        with np.errstate(invalid="ignore", divide="ignore"):
+            w = w / w.sum(axis=1, keepdims=True)
+    w = w * scale
+    w[bad] = np.nan
+    return w
+
+
+def selected_router_backward(logits: np.ndarray, idx: np.ndarray, grad_w: np.ndarray,
+                             scoring: str, renormalize: bool, scale: float) -> np.ndarray:
+    """dL/dlogits [T, E] of selected_router_weights given dL/dw [T, k] (chain rule, float64).
+
+    With q_j the selected score (p or s) of slot j, G_e = sum over slots j with idx j = e of g_j,
+    and for renormalisation Z = sum_j q_j:
+      softmax, plain:  dl_e = scale * p_e * (G_e - sum_j g_j q_j)
+      softmax, renorm: the weights are a softmax over the k selected logits, r_j = q_j / Z:
+                       dl_e = scale * (sum_{j: idx_j = e} g_j r_j - n_e r_e * sum_j g_j r_j)
+                       where n_e counts the slots holding e and r_e = p_e / Z
+      sigmoid, plain:  dl_e = scale * s_e (1 - s_e) * G_e
+      sigmoid, renorm: dl_e = scale * s_e (1 - s_e) / Z * (G_e - n_e * sum_j g_j q_j / Z)
+    Rows with an invalid index are all NaN.
+    """
+    T, E = logits.shape
+    idx = np.asarray(idx).astype(np.int64)
+    bad = ((idx < 0) | (idx >= E)).any(axis=1)
+    sidx = np.where(idx < 0, 0, np.minimum(idx, E - 1))
+    g = np.asarray(grad_w, dtype=np.float64)
+    p = _selection_scores(logits, scoring)
+    q = np.take_along_axis(p, sidx, axis=1)
+    rows = np.arange(T)[:, None]
+    G = np.zeros((T, E))
+    np.add.at(G, (np.broadcast_to(rows, sidx.shape), sidx), g)
+    n = np.zeros((T, E))
+    np.add.at(n, (np.broadcast_to(rows, sidx.shape), sidx), 1.0)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        if scoring == "softmax" and not renormalize:
+            out = p * (G - (g * q).sum(axis=1, keepdims=True))
+        elif scoring == "softmax":
+            Z = q.sum(axis=1, keepdims=True)
+            r = q / Z
+            Gr = np.zeros((T, E))
+            np.add.at(Gr, (np.broadcast_to(rows, sidx.shape), sidx), g * r)
+            out = Gr - n * (p / Z) * (g * r).sum(axis=1, keepdims=True)
+        elif not renormalize:
+            out = p * (1.0 - p) * G
+        else:
+            Z = q.sum(axis=1, keepdims=True)
+            out = p * (1.0 - p) / Z * (G - n * (g * q).sum(axis=1, keepdims=True) / Z)
+    out = out * scale
+    out[bad] = np.nan
+    return out
