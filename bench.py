@@ -457,7 +457,9 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (x %.0f MB, weights %.1f GB); no flush" % (
                            x.numel() * 2 / 1e6, 3 * gate.numel() * 2 / 1e9),
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"kernel": "moe_experts_tc<gate/up> (tcgen05 grouped GEMM + SwiGLU)",
+            "roofline": {"kernel": ("moe_experts_tc2<gate/up> (CTA-pair tcgen05 grouped GEMM + SwiGLU)"
+                                    if wl.rows >= 128 * wl.E else
+                                    "moe_experts_tc<gate/up> (tcgen05 grouped GEMM + SwiGLU)"),
                          "bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
                          "peak_source": f"{pk_src} bf16 sustained",

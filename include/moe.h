@@ -49,6 +49,8 @@ typedef enum {
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_F16 = 1, MOE_BF16 = 2 } moe_dtype;
+typedef enum { MOE_IDX_U32 = 0, MOE_IDX_I32 = 1, MOE_IDX_I64 = 2 } moe_index_dtype;
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_scoring;
 
 /* Static text for a status code (never NULL). */
 const char* moe_status_string(int status);
@@ -93,6 +95,34 @@ int moe_route_sigmoid_grouped(const void* logits, int ldt, const float* bias, in
                               int64_t E, int top_k, int groups, int selected_groups,
                               int group_top_two, int renormalize, float scale, uint32_t* idx,
                               void* w, moe_stream_t stream);
+
+/*
+ * moe_selected_router_weights — selected_router_weights(logits, indices, RouterWeightOptions) of
+ * §12 "MoE-Training erster Ordnung": the continuous weights of a FIXED selection.
+ *
+ * For slot j of row t with expert i = idx[t, j]: q = p[t, i], p the softmax over all E experts
+ * (scoring = MOE_SCORE_SOFTMAX, FP32) or sigmoid(logit) (MOE_SCORE_SIGMOID).
+ * w[t, j] = scale * q, or scale * q / sum_j q with renormalize != 0.  Repeated indices gather the
+ * same q.  A row holding an index outside [0, E) (or, with softmax, a NaN / +inf / only -inf
+ * logit) is all NaN; out-of-range indices are never dereferenced and nothing is synchronised.
+ * logits [T, E] dtype ldt; idx [T, top_k] of index dtype idt; w [T, top_k] FP32.
+ * Limits: 1 <= top_k <= min(E, 64), E <= 1024; scale finite and > 0 (else MOE_ERR_ARG).
+ */
+int moe_selected_router_weights(const void* logits, int ldt, const void* idx, int idt, int64_t T,
+                                int64_t E, int top_k, int scoring, int renormalize, float scale,
+                                float* w, moe_stream_t stream);
+
+/*
+ * moe_selected_router_backward — selected_router_backward(logits, indices, grad_weights, options)
+ * of §12: dL/dlogits [T, E] (dtype ldt) of the weights above for dL/dw = grad_w [T, top_k] (FP32).
+ * Only the continuous weights are differentiated, not the top-k / group decisions or a bias.
+ * Rows that are NaN in the forward are NaN here.  Per-expert sums over repeated indices are
+ * accumulated in slot order (run-to-run identical).  Same limits as the forward.
+ */
+int moe_selected_router_backward(const void* logits, int ldt, const void* idx, int idt,
+                                 const float* grad_w, int64_t T, int64_t E, int top_k, int scoring,
+                                 int renormalize, float scale, void* grad_logits,
+                                 moe_stream_t stream);
 
 /*
  * moe_dispatch — RoutingPlan::dispatch(input) of §3/§5 "Expertengewichte und Verteilung".

@@ -31,6 +31,10 @@ _SIGS = {
     "moe_route": (_int, [_vp, _int, _i64, _i64, _int, _int, _vp, _vp, _vp]),
     "moe_route_sigmoid_grouped": (_int, [_vp, _int, _vp, _i64, _i64, _int, _int, _int, _int, _int,
                                          _f32, _vp, _vp, _vp]),
+    "moe_selected_router_weights": (_int, [_vp, _int, _vp, _int, _i64, _i64, _int, _int, _int,
+                                           _f32, _vp, _vp]),
+    "moe_selected_router_backward": (_int, [_vp, _int, _vp, _int, _vp, _i64, _i64, _int, _int,
+                                            _int, _f32, _vp, _vp]),
     "moe_dispatch_workspace_bytes": (_sz, [_i64, _i64, _int]),
     "moe_dispatch": (_int, [_vp, _int, _i64, _i64, _vp, _i64, _int, _vp, _vp, _vp, _vp, _vp, _sz,
                             _vp]),
@@ -143,6 +147,43 @@ def moe_route_sigmoid_grouped(logits, top_k: int, groups: int, selected_groups: 
         int(bool(group_top_two)), int(bool(renormalize)), float(scale), _ptr(idx), _ptr(w),
         _stream(stream)), "moe_route_sigmoid_grouped")
     return idx, w
+
+
+INDEX_CODE = {torch.uint32: 0, torch.int32: 1, torch.int64: 2}
+SCORING = {"softmax": 0, "sigmoid": 1}
+
+
+def moe_selected_router_weights(logits, idx, scoring: str = "softmax", renormalize: bool = True,
+                                scale: float = 1.0, w=None, stream=None):
+    """selected_router_weights(logits, indices, options) -> FP32 weights [T, k]."""
+    _cuda(logits, idx)
+    T, E = logits.shape
+    k = idx.shape[1]
+    w = torch.empty(T, k, dtype=torch.float32, device=logits.device) if w is None else w
+    _cuda(w)
+    _check(lib().moe_selected_router_weights(
+        _ptr(logits), _code(logits), _ptr(idx), INDEX_CODE[idx.dtype], T, E, k, SCORING[scoring],
+        int(bool(renormalize)), float(scale), _ptr(w), _stream(stream)),
+        "moe_selected_router_weights")
+    return w
+
+
+def moe_selected_router_backward(logits, idx, grad_w, scoring: str = "softmax",
+                                 renormalize: bool = True, scale: float = 1.0, grad=None,
+                                 stream=None):
+    """selected_router_backward(logits, indices, grad_weights, options) -> dL/dlogits [T, E]."""
+    _cuda(logits, idx, grad_w)
+    if grad_w.dtype != torch.float32:
+        raise MoeError(3, "grad_weights must be float32")
+    T, E = logits.shape
+    k = idx.shape[1]
+    grad = torch.empty_like(logits) if grad is None else grad
+    _cuda(grad)
+    _check(lib().moe_selected_router_backward(
+        _ptr(logits), _code(logits), _ptr(idx), INDEX_CODE[idx.dtype], _ptr(grad_w), T, E, k,
+        SCORING[scoring], int(bool(renormalize)), float(scale), _ptr(grad), _stream(stream)),
+        "moe_selected_router_backward")
+    return grad
 
 
 def dispatch_workspace_bytes(T: int, E: int, top_k: int) -> int:

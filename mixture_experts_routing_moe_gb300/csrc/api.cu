@@ -201,6 +201,42 @@ int moe_route_sigmoid_grouped(const void* logits, int ldt, const float* bias, in
                                           scale, idx, w, (cudaStream_t)stream));
 }
 
+static int check_router_train(int ldt, int idt, int64_t T, int64_t E, int top_k, int scoring,
+                              float scale) {
+  if (!valid_dtype(ldt)) return MOE_ERR_DTYPE;
+  if (idt != MOE_IDX_U32 && idt != MOE_IDX_I32 && idt != MOE_IDX_I64) return MOE_ERR_DTYPE;
+  if (scoring != MOE_SCORE_SOFTMAX && scoring != MOE_SCORE_SIGMOID) return MOE_ERR_ARG;
+  if (T < 0 || E < 1 || E > kMaxE || top_k < 1 || top_k > 64 || top_k > E) return MOE_ERR_SHAPE;
+  if (T * top_k >= kMaxRows || T * E >= ((int64_t)1 << 40)) return MOE_ERR_SHAPE;
+  if (!(scale > 0.f) || !isfinite(scale)) return MOE_ERR_ARG;
+  return MOE_OK;
+}
+
+int moe_selected_router_weights(const void* logits, int ldt, const void* idx, int idt, int64_t T,
+                                int64_t E, int top_k, int scoring, int renormalize, float scale,
+                                float* w, moe_stream_t stream) {
+  const int st = check_router_train(ldt, idt, T, E, top_k, scoring, scale);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!logits || !idx || !w) return MOE_ERR_NULL;
+  return cuda_status(launch_router_train(logits, ldt, idx, idt, nullptr, T, (int)E, top_k,
+                                         scoring, renormalize != 0, scale, w, nullptr,
+                                         (cudaStream_t)stream));
+}
+
+int moe_selected_router_backward(const void* logits, int ldt, const void* idx, int idt,
+                                 const float* grad_w, int64_t T, int64_t E, int top_k, int scoring,
+                                 int renormalize, float scale, void* grad_logits,
+                                 moe_stream_t stream) {
+  const int st = check_router_train(ldt, idt, T, E, top_k, scoring, scale);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  if (!logits || !idx || !grad_w || !grad_logits) return MOE_ERR_NULL;
+  return cuda_status(launch_router_train(logits, ldt, idx, idt, grad_w, T, (int)E, top_k, scoring,
+                                         renormalize != 0, scale, nullptr, grad_logits,
+                                         (cudaStream_t)stream));
+}
+
 size_t moe_dispatch_workspace_bytes(int64_t T, int64_t E, int top_k) {
   if (check_route_shape(T, E, top_k) != MOE_OK) return 0;
   return align_up(kWsHeader, 256) + dispatch_scratch_bytes(T * top_k, (int)E);

@@ -116,11 +116,6 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
   asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -287,18 +282,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, armed = 0;
       uint32_t phase = 0;
       bool stop = false;
-#ifndef MOE_TC_HINTS
-#define MOE_TC_HINTS 1
-#endif
       // The resident operand is marked evict_last.  The other one is NOT marked evict_first:
       // each of its tiles is still read by every CTA of the same m-row / n-column, shortly apart.
-      const uint64_t keep = policy_evict_last(),
-                     other = MOE_TC_HINTS == 2 ? policy_evict_first() : policy_evict_normal();
+      const uint64_t keep = policy_evict_last(), other = policy_evict_normal();
       for (int t = blockIdx.x; t < total && !stop; t += gridDim.x) {
         int e, m, n;
         const bool a_res = decode_tile(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
-        uint64_t pa = a_res ? keep : other, pb = a_res ? other : keep;
-        if (MOE_TC_HINTS == 0) pa = pb = policy_evict_normal();
+        const uint64_t pa = a_res ? keep : other, pb = a_res ? other : keep;
         const int a_row = __ldg(p.offsets + e) + m * BM;
         const int b_row = e * p.b_rows + n * (GATEUP ? BN / 2 : BN);
         for (int kb = 0; kb < p.KB; ++kb) {

@@ -22,6 +22,11 @@ cudaError_t launch_route_sigmoid(const void* logits, int ldt, const float* bias,
                                  int k, int G, int SG, int top_two, int renorm, float scale,
                                  uint32_t* idx, void* w, cudaStream_t s);
 
+// Fixed-selection router weights (grad_w == nullptr) or their logits gradient.
+cudaError_t launch_router_train(const void* logits, int ldt, const void* idx, int idt,
+                                const float* grad_w, int64_t T, int E, int k, int scoring,
+                                int renorm, float scale, float* w, void* grad, cudaStream_t s);
+
 // Dispatch splits the R = T*k slots into W contiguous chunks of CH slots, one per warp.
 struct DispatchPlan {
   int W;   // chunks (warps)

@@ -22,7 +22,7 @@ F32, F16, BF16 = B.MOE_F32, B.MOE_F16, B.MOE_BF16
 
 def test_exports_every_header_function(L):
     names = B.header_functions()
-    assert len(names) == 15
+    assert len(names) == 17
     for n in names:
         assert hasattr(L, n), n
     assert L.moe_abi_version() == 1
@@ -140,3 +140,19 @@ def test_sigmoid_router_rejects(L):
     assert L.moe_forward_sigmoid_grouped(FAKE, FAKE, BF16, None, FAKE, FAKE, FAKE, BF16, 16, 64,
                                          128, 256, 8, 8, 4, 1, 1, -1.0, FAKE, FAKE, need,
                                          None) == 9
+
+
+def test_router_train_rejects(L):
+    def fw(ldt=F32, idt=0, T=8, E=16, k=4, sc=0, scale=1.0, logits=FAKE):
+        return L.moe_selected_router_weights(logits, ldt, FAKE, idt, T, E, k, sc, 1, scale, FAKE,
+                                             None)
+    assert fw(ldt=4) == 3
+    assert fw(idt=3) == 3
+    assert fw(sc=2) == 9
+    assert fw(k=17) == 2
+    assert fw(k=65, E=128) == 2
+    assert fw(scale=-2.0) == 9
+    assert fw(logits=None) == 1
+    assert fw(T=0, logits=None) == 0
+    assert L.moe_selected_router_backward(FAKE, F32, FAKE, 2, None, 8, 16, 4, 1, 0, 1.0, FAKE,
+                                          None) == 1
