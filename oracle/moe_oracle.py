@@ -49,6 +49,14 @@ FP32 weights [T, k] for given indices (softmax over all experts, or sigmoid), op
 renormalisation over the k slots, then `scale`; repeated indices gather; an invalid index makes
 the whole row NaN; the gradient is with respect to the logits of the continuous weights only.
 
+The backward chain of the same section (combine_backward -> expert backward ->
+dispatch_backward, then the router backward above) is the chain rule of the forward written out:
+  combine:  dexpert[row(t, j)] = w[t, j] * dout[t];  dweights[t, j] = <dout[t], y[row(t, j)]>
+  experts:  da = dy down_e;  du = da * silu(g);  dg = da * u * silu'(g),
+            silu'(g) = s (1 + g (1 - s)), s = sigmoid(g);  dx = dg gate_e + du up_e;
+            ddown_e = dy^T a;  dgate_e = dg^T x;  dup_e = du^T x
+  dispatch: dx[t] = sum_j dinput[row(t, j)]  (the routing weights are not applied again)
+
 Pins (tests/test_oracle_pins.py) tie each function to something other than itself: closed forms,
 library routines (torch float64 softmax and silu, numpy's float32 cast), brute force on tiny
 inputs, and invariants.  Parity unpinned: R1 for two *different* logits whose FP32 softmax values
@@ -62,7 +70,8 @@ __all__ = [
     "DTYPES", "to_f64", "round_to_dtype", "encode", "poisoned_rows", "softmax", "select_topk",
     "route", "dispatch", "gather", "silu", "swiglu", "experts", "combine", "forward",
     "forward_rows", "sigmoid", "route_sigmoid_grouped", "forward_sigmoid_grouped",
-    "selected_router_weights", "selected_router_backward",
+    "selected_router_weights", "selected_router_backward", "combine_backward",
+    "experts_backward", "dispatch_backward",
 ]
 
 DTYPES = ("f32", "f16", "bf16")
@@ -428,3 +437,58 @@ def selected_router_backward(logits: np.ndarray, idx: np.ndarray, grad_w: np.nda
     out = out * scale
     out[bad] = np.nan
     return out
+
+
+# --------------------------------------------------------------------------------------------
+# backward chain (§12 "MoE-Training erster Ordnung", steps 1-3)
+# --------------------------------------------------------------------------------------------
+def combine_backward(y: np.ndarray, row_of_slot: np.ndarray, w: np.ndarray, dout: np.ndarray):
+    """dexpert [T*k, H] and dweights [T, k] of out[t] = sum_j w[t, j] y[row(t, j)]."""
+    T, k = w.shape
+    rs = row_of_slot.astype(np.int64).reshape(T, k)
+    dexpert = np.zeros_like(y, dtype=np.float64)
+    dweights = np.zeros((T, k))
+    for j in range(k):
+        dexpert[rs[:, j]] = w[:, j:j + 1] * dout
+        dweights[:, j] = (dout * y[rs[:, j]]).sum(axis=1)
+    return dexpert, dweights
+
+
+def experts_backward(x_d: np.ndarray, offsets, gate, up, down, wdtype: str, dy: np.ndarray):
+    """Gradients of forward_dispatched for dL/dy: (dinput [rows, H], dgate [E, I, H],
+    dup [E, I, H], ddown [E, H, I]), all float64, recomputing g = x gate^T and u = x up^T."""
+    E = len(offsets) - 1
+    I, H = gate.shape[1], gate.shape[2]
+    dx = np.zeros_like(x_d, dtype=np.float64)
+    dgate = np.zeros((E, I, H))
+    dup = np.zeros((E, I, H))
+    ddown = np.zeros((E, H, I))
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi <= lo:
+            continue
+        ge, ue, de = (to_f64(wt[e], wdtype) for wt in (gate, up, down))
+        x = x_d[lo:hi]
+        g = x @ ge.T
+        u = x @ ue.T
+        with np.errstate(over="ignore"):
+            s = 1.0 / (1.0 + np.exp(-g))
+        act = g * s
+        a = act * u
+        da = dy[lo:hi] @ de
+        du = da * act
+        dg = da * u * (s * (1.0 + g * (1.0 - s)))
+        dx[lo:hi] = dg @ ge + du @ ue
+        ddown[e] = dy[lo:hi].T @ a
+        dgate[e] = dg.T @ x
+        dup[e] = du.T @ x
+    return dx, dgate, dup, ddown
+
+
+def dispatch_backward(dinput: np.ndarray, row_of_slot: np.ndarray, T: int, k: int):
+    """dx [T, H] = sum over the k slots of each token of its dispatched rows' gradients."""
+    rs = row_of_slot.astype(np.int64).reshape(T, k)
+    dx = np.zeros((T, dinput.shape[1]))
+    for j in range(k):
+        dx += dinput[rs[:, j]]
+    return dx
