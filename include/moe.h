@@ -230,6 +230,43 @@ int moe_forward_sigmoid_grouped(const void* x, const void* logits, int ldt, cons
                                 moe_stream_t stream);
 
 /*
+ * Backward chain of §12 "MoE-Training erster Ordnung" (first order).  The forward saves nothing
+ * beyond its inputs: the expert backward recomputes g = x_d gate^T and u = x_d up^T from x_d, so
+ * the "cache" of forward_dispatched_training is (x_d, offsets) as returned by moe_dispatch.
+ *
+ * moe_combine_backward — DispatchedTokens::combine_backward(expert_output, grad_output):
+ *   dexpert[row_of_slot[t*k+j]] = w[t, j] * dout[t]   ([T*k, H], dtype ydt; rows of slots whose
+ *                                                       row_of_slot is 0xFFFFFFFF are skipped)
+ *   dweights[t, j] = sum_h dout[t, h] * y[row_of_slot[t*k+j], h]   ([T, k] FP32, NaN for such slots)
+ *   y [T*k, H] the expert output, w [T, k] the routing weights (dtype wdt), dout [T, H] dtype ydt.
+ */
+int moe_combine_backward(const void* y, int ydt, const uint32_t* row_of_slot, const void* w,
+                         int wdt, const void* dout, int64_t T, int64_t H, int top_k,
+                         void* dexpert, float* dweights, moe_stream_t stream);
+
+/*
+ * moe_experts_backward — cache.backward(dexpert): for every expert e and its rows,
+ *   da = dy down_e;  s = sigmoid(g);  du = da * g s;  dg = da * u * s (1 + g (1 - s))
+ *   dinput = dg gate_e + du up_e                 ([rows, H], dtype wdt)
+ *   ddown[e] = dy^T (g s u); dgate[e] = dg^T x_d; dup[e] = du^T x_d   (FP32, [E,H,I], [E,I,H] x2)
+ * computed with FP32 accumulation on CUDA cores.  Experts without rows get zero gradients.
+ * dy [rows, H] dtype wdt.  ws: moe_experts_backward_workspace_bytes(rows, I), 256-byte aligned.
+ */
+size_t moe_experts_backward_workspace_bytes(int64_t rows, int64_t I);
+int moe_experts_backward(const void* x_d, const int32_t* offsets, int64_t rows, const void* gate,
+                         const void* up, const void* down, int wdt, int64_t E, int64_t H,
+                         int64_t I, const void* dy, void* dinput, float* dgate, float* dup,
+                         float* ddown, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_dispatch_backward — DispatchedTokens::dispatch_backward(dinput): dx[t] = sum over the slots
+ * j of token t of dinput[row_of_slot[t*k+j]], FP32 in slot order, rounded to `dt`; the routing
+ * weights are not applied again.  dinput [T*k, H], dx [T, H], both dtype dt.
+ */
+int moe_dispatch_backward(const void* dinput, int dt, const uint32_t* row_of_slot, int64_t T,
+                          int64_t H, int top_k, void* dx, moe_stream_t stream);
+
+/*
  * moe_forward_with_events — moe_forward that also records caller-created CUDA events
  * (cudaEvent_t, passed as void*) on `stream` at the stage boundaries, for timing:
  *   events[0] before the route      events[1] after the route     events[2] after dispatch

@@ -52,6 +52,12 @@ _SIGS = {
                                            _vp, _sz, _vp]),
     "moe_forward_with_events": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _int, _i64, _i64, _i64,
                                        _i64, _int, _int, _vp, _vp, _sz, _vp, _vp]),
+    "moe_combine_backward": (_int, [_vp, _int, _vp, _vp, _int, _vp, _i64, _i64, _int, _vp, _vp,
+                                    _vp]),
+    "moe_experts_backward_workspace_bytes": (_sz, [_i64, _i64]),
+    "moe_experts_backward": (_int, [_vp, _vp, _i64, _vp, _vp, _vp, _int, _i64, _i64, _i64, _vp,
+                                    _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_dispatch_backward": (_int, [_vp, _int, _vp, _i64, _i64, _int, _vp, _vp]),
     "moe_device_status": (_int, [_vp, _sz, _vp]),
 }
 
@@ -307,6 +313,49 @@ def moe_forward_with_events(x, logits, gate, up, down, top_k: int, renormalize: 
         H, I, top_k, int(bool(renormalize)), _ptr(out), _ptr(ws), ws.numel(), _stream(stream),
         arr), "moe_forward_with_events")
     return out
+
+
+def moe_combine_backward(y, row_of_slot, w, dout, stream=None):
+    """DispatchedTokens::combine_backward -> (dexpert [T*k, H], dweights [T, k] FP32)."""
+    _cuda(y, row_of_slot, w, dout)
+    T, k = w.shape
+    H = y.shape[1]
+    dexpert = torch.zeros_like(y)
+    dweights = torch.empty(T, k, dtype=torch.float32, device=y.device)
+    _check(lib().moe_combine_backward(_ptr(y), _code(y), _ptr(row_of_slot), _ptr(w), _code(w),
+                                      _ptr(dout), T, H, k, _ptr(dexpert), _ptr(dweights),
+                                      _stream(stream)), "moe_combine_backward")
+    return dexpert, dweights
+
+
+def moe_experts_backward(x_d, offsets, gate, up, down, dy, ws=None, stream=None):
+    """cache.backward(dexpert) -> (dinput [rows, H], dgate, dup [E, I, H], ddown [E, H, I] FP32)."""
+    _cuda(x_d, offsets, gate, up, down, dy)
+    rows, H = x_d.shape
+    E, I, _ = gate.shape
+    dev = x_d.device
+    dinput = torch.empty_like(x_d)
+    dgate = torch.empty(E, I, H, dtype=torch.float32, device=dev)
+    dup = torch.empty(E, I, H, dtype=torch.float32, device=dev)
+    ddown = torch.empty(E, H, I, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = torch.empty(max(lib().moe_experts_backward_workspace_bytes(rows, I), 256),
+                         dtype=torch.uint8, device=dev)
+    _check(lib().moe_experts_backward(
+        _ptr(x_d), _ptr(offsets), rows, _ptr(gate), _ptr(up), _ptr(down), _code(gate), E, H, I,
+        _ptr(dy), _ptr(dinput), _ptr(dgate), _ptr(dup), _ptr(ddown), _ptr(ws), ws.numel(),
+        _stream(stream)), "moe_experts_backward")
+    return dinput, dgate, dup, ddown
+
+
+def moe_dispatch_backward(dinput, row_of_slot, T: int, top_k: int, stream=None):
+    """DispatchedTokens::dispatch_backward -> dx [T, H] (slot rows summed, no weights)."""
+    _cuda(dinput, row_of_slot)
+    H = dinput.shape[1]
+    dx = torch.empty(T, H, dtype=dinput.dtype, device=dinput.device)
+    _check(lib().moe_dispatch_backward(_ptr(dinput), _code(dinput), _ptr(row_of_slot), T, H, top_k,
+                                       _ptr(dx), _stream(stream)), "moe_dispatch_backward")
+    return dx
 
 
 def moe_device_status(ws, stream=None) -> int:

@@ -366,6 +366,57 @@ int moe_forward_sigmoid_grouped(const void* x, const void* logits, int ldt, cons
                      (cudaStream_t)stream, nullptr);
 }
 
+int moe_combine_backward(const void* y, int ydt, const uint32_t* row_of_slot, const void* w,
+                         int wdt, const void* dout, int64_t T, int64_t H, int top_k,
+                         void* dexpert, float* dweights, moe_stream_t stream) {
+  if (!valid_dtype(ydt) || !valid_dtype(wdt)) return MOE_ERR_DTYPE;
+  if (T < 0 || H < 1 || top_k < 1 || top_k > kMaxE || T * top_k >= kMaxRows) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!y || !row_of_slot || !w || !dout || !dexpert || !dweights) return MOE_ERR_NULL;
+  return cuda_status(launch_combine_backward(y, ydt, row_of_slot, w, wdt, dout, T, H, top_k,
+                                             dexpert, dweights, (cudaStream_t)stream));
+}
+
+size_t moe_experts_backward_workspace_bytes(int64_t rows, int64_t I) {
+  if (rows < 0 || rows >= kMaxRows || I < 1) return 0;
+  return align_up(kWsHeader, 256) + align_up(experts_backward_scratch_bytes(rows, I), 256);
+}
+
+int moe_experts_backward(const void* x_d, const int32_t* offsets, int64_t rows, const void* gate,
+                         const void* up, const void* down, int wdt, int64_t E, int64_t H,
+                         int64_t I, const void* dy, void* dinput, float* dgate, float* dup,
+                         float* ddown, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!valid_dtype(wdt)) return MOE_ERR_DTYPE;
+  const int st = check_experts_shape(rows, E, H, I);
+  if (st != MOE_OK) return st;
+  if (!gate || !up || !down || !dgate || !dup || !ddown) return MOE_ERR_NULL;
+  if (rows > 0 && (!x_d || !offsets || !dy || !dinput)) return MOE_ERR_NULL;
+  if (!ws || ((uintptr_t)ws & 255u) != 0 || ws_bytes < moe_experts_backward_workspace_bytes(rows, I))
+    return MOE_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (rows == 0) {  // no rows: every weight gradient is zero
+    const size_t n = (size_t)E * H * I * sizeof(float);
+    if (cudaMemsetAsync(dgate, 0, n, s) != cudaSuccess || cudaMemsetAsync(dup, 0, n, s) != cudaSuccess ||
+        cudaMemsetAsync(ddown, 0, n, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  float* scratch = (float*)((uint8_t*)ws + align_up(kWsHeader, 256));
+  return cuda_status(launch_experts_backward(x_d, offsets, rows, gate, up, down, wdt, (int)E,
+                                             (int)H, (int)I, dy, dinput, dgate, dup, ddown,
+                                             scratch, s));
+}
+
+int moe_dispatch_backward(const void* dinput, int dt, const uint32_t* row_of_slot, int64_t T,
+                          int64_t H, int top_k, void* dx, moe_stream_t stream) {
+  if (!valid_dtype(dt)) return MOE_ERR_DTYPE;
+  if (T < 0 || H < 1 || top_k < 1 || top_k > kMaxE || T * top_k >= kMaxRows) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!dinput || !row_of_slot || !dx) return MOE_ERR_NULL;
+  return cuda_status(launch_dispatch_backward(dinput, dt, row_of_slot, T, H, top_k, dx,
+                                              (cudaStream_t)stream));
+}
+
 int moe_device_status(void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!ws || ws_bytes < sizeof(unsigned)) return MOE_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;

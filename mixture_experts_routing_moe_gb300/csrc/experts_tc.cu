@@ -20,7 +20,7 @@
 //              to the expert's rows and to the valid columns.
 // Tiles are (expert, m-tile, n-tile); the list is derived on the device from the offsets.  Within
 // an expert the smaller operand (the expert's rows of x_d / a, or its weights) stays resident in
-// L2 (evict_last) while the larger one streams through once (evict_first).
+// L2 (evict_last) while the larger one streams through it (evict_normal).
 // Every wait on an mbarrier is bounded (about a second); on expiry the CTA records the timeout in
 // the status word, stops issuing, lets in-flight copies and MMAs land, frees TMEM and exits.
 #include <cuda.h>

@@ -27,6 +27,19 @@ cudaError_t launch_router_train(const void* logits, int ldt, const void* idx, in
                                 const float* grad_w, int64_t T, int E, int k, int scoring,
                                 int renorm, float scale, float* w, void* grad, cudaStream_t s);
 
+// Backward chain (FP32 CUDA-core GEMMs for the experts).
+size_t experts_backward_scratch_bytes(int64_t rows, int64_t I);
+cudaError_t launch_experts_backward(const void* x_d, const int32_t* offsets, int64_t rows,
+                                    const void* gate, const void* up, const void* down, int wdt,
+                                    int E, int H, int I, const void* dy, void* dinput,
+                                    float* dgate, float* dup, float* ddown, float* scratch,
+                                    cudaStream_t s);
+cudaError_t launch_combine_backward(const void* y, int ydt, const uint32_t* ros, const void* w,
+                                    int wdt, const void* dout, int64_t T, int64_t H, int k,
+                                    void* dexpert, float* dweights, cudaStream_t s);
+cudaError_t launch_dispatch_backward(const void* dinput, int dt, const uint32_t* ros, int64_t T,
+                                     int64_t H, int k, void* dx, cudaStream_t s);
+
 // Dispatch splits the R = T*k slots into W contiguous chunks of CH slots, one per warp.
 struct DispatchPlan {
   int W;   // chunks (warps)

@@ -22,7 +22,7 @@ F32, F16, BF16 = B.MOE_F32, B.MOE_F16, B.MOE_BF16
 
 def test_exports_every_header_function(L):
     names = B.header_functions()
-    assert len(names) == 17
+    assert len(names) == 21
     for n in names:
         assert hasattr(L, n), n
     assert L.moe_abi_version() == 1
@@ -156,3 +156,15 @@ def test_router_train_rejects(L):
     assert fw(T=0, logits=None) == 0
     assert L.moe_selected_router_backward(FAKE, F32, FAKE, 2, None, 8, 16, 4, 1, 0, 1.0, FAKE,
                                           None) == 1
+
+
+def test_backward_chain_rejects(L):
+    assert L.moe_combine_backward(FAKE, 5, FAKE, FAKE, F32, FAKE, 4, 8, 2, FAKE, FAKE, None) == 3
+    assert L.moe_combine_backward(FAKE, F32, FAKE, FAKE, F32, None, 4, 8, 2, FAKE, FAKE, None) == 1
+    assert L.moe_dispatch_backward(FAKE, BF16, FAKE, 4, 0, 2, FAKE, None) == 2
+    need = L.moe_experts_backward_workspace_bytes(64, 32)
+    assert need >= 256 + 64 * 32 * 20
+    assert L.moe_experts_backward(FAKE, FAKE, 64, FAKE, FAKE, FAKE, BF16, 4, 16, 32, FAKE, FAKE,
+                                  FAKE, FAKE, FAKE, FAKE, need - 1, None) == 5
+    assert L.moe_experts_backward(FAKE, FAKE, 64, FAKE, FAKE, FAKE, BF16, 4, 16, 32, None, FAKE,
+                                  FAKE, FAKE, FAKE, FAKE, need, None) == 1

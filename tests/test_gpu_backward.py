@@ -1,0 +1,111 @@
+"""GPU parity of the MoE backward chain (ruDNN user guide §12) against the fp64 oracle:
+combine_backward, the expert backward (dinput, FP32 dgate / dup / ddown), dispatch_backward and
+the full chain with the router backward.  Bounds: FP32 outputs (weight gradients, dweights)
+within 1e-4 of the largest |ref|; layer-dtype outputs within the layer tolerance (2e-2 for
+16-bit, 1e-4 for f32) of the largest |ref|."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import mixture_experts_routing_moe_gb300 as moe
+from mixture_experts_routing_moe_gb300 import workloads as W
+from gpu_helpers import DT_NAME, f64, layer_tol, rel_max_err, storage, u32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _groups(counts, seed):
+    rng = np.random.default_rng(seed)
+    ids = np.concatenate([np.full(n, e) for e, n in enumerate(counts)])
+    rng.shuffle(ids)
+    return ids.astype(np.uint32)[:, None]
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("counts,H,I", [([70, 0, 129, 5], 96, 160), ([200], 64, 72),
+                                        ([33] * 6, 128, 256), ([0, 0, 3, 0], 40, 24)])
+def test_experts_backward_matches_oracle(dt, counts, H, I):
+    E = len(counts)
+    _, offsets, _, _ = O.dispatch(_groups(counts, sum(counts)), E)
+    rows = int(offsets[-1])
+    g = torch.Generator().manual_seed(rows + H + I)
+    x_d = torch.randn(rows, H, generator=g).to(dt)
+    gate = (torch.randn(E, I, H, generator=g) / H ** 0.5).to(dt)
+    up = (torch.randn(E, I, H, generator=g) / H ** 0.5).to(dt)
+    down = (torch.randn(E, H, I, generator=g) / I ** 0.5).to(dt)
+    dy = torch.randn(rows, H, generator=g).to(dt)
+    off_t = torch.from_numpy(offsets.astype(np.int32)).to(DEV)
+    dx, dg, du, dd = moe.moe_experts_backward(x_d.to(DEV), off_t, gate.to(DEV), up.to(DEV),
+                                              down.to(DEV), dy.to(DEV))
+    torch.cuda.synchronize()
+    name = DT_NAME[dt]
+    rdx, rdg, rdu, rdd = O.experts_backward(O.to_f64(*storage(x_d)), offsets, storage(gate)[0],
+                                            storage(up)[0], storage(down)[0], name,
+                                            O.to_f64(*storage(dy)))
+    assert rel_max_err(f64(dx), rdx) <= layer_tol(dt)
+    for got, ref in ((dg, rdg), (du, rdu), (dd, rdd)):
+        assert rel_max_err(f64(got), ref) <= 1e-4
+
+
+@pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
+def test_combine_and_dispatch_backward_match_oracle(ydt):
+    T, k, H, E = 150, 3, 96, 7
+    gen = torch.Generator().manual_seed(5)
+    idx = torch.stack([torch.randperm(E, generator=gen)[:k] for _ in range(T)]).numpy().astype(np.uint32)
+    _, _, _, ros = O.dispatch(idx, E)
+    y = torch.randn(T * k, H, generator=gen).to(ydt)
+    w = torch.rand(T, k, generator=gen).to(ydt)
+    dout = torch.randn(T, H, generator=gen).to(ydt)
+    ros_t = torch.from_numpy(ros.view(np.int32)).to(DEV).view(torch.uint32)
+    de, dw = moe.moe_combine_backward(y.to(DEV), ros_t, w.to(DEV), dout.to(DEV))
+    rde, rdw = O.combine_backward(O.to_f64(*storage(y)), ros, O.to_f64(*storage(w)),
+                                  O.to_f64(*storage(dout)))
+    assert rel_max_err(f64(de), rde) <= (1e-6 if ydt == torch.float32 else 2.0 ** -8)
+    assert rel_max_err(f64(dw), rdw) <= 1e-5
+    dx = moe.moe_dispatch_backward(de, ros_t, T, k)
+    rdx = O.dispatch_backward(O.to_f64(*storage(de.cpu())), ros, T, k)
+    assert rel_max_err(f64(dx), rdx) <= (1e-6 if ydt == torch.float32 else 2.0 ** -8)
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_full_backward_chain_matches_oracle(dt):
+    """forward (route, dispatch, experts, combine) then combine_backward -> experts backward ->
+    dispatch_backward -> router backward, against the oracle's chain on the same stored values."""
+    wl = W.Workload("bwd_layer", T=200, H=128, I=192, E=8, top_k=2, renormalize=True,
+                    dtype=DT_NAME[dt], seed=41)
+    inp = W.make_layer_inputs(wl, "cpu")
+    gdev = {k: v.to(DEV) for k, v in inp.items()}
+    dout = torch.randn(wl.T, wl.H, generator=torch.Generator().manual_seed(6)).to(dt)
+    idx, w = moe.moe_route(gdev["logits"], wl.top_k, True)
+    d = moe.moe_dispatch(gdev["x"], idx, wl.E)
+    y = moe.moe_experts_forward_dispatched(d["x_d"], d["offsets"], gdev["gate"], gdev["up"],
+                                           gdev["down"])
+    wts = moe.moe_selected_router_weights(gdev["logits"], idx, "softmax", True, 1.0)
+    de, dwts = moe.moe_combine_backward(y, d["row_of_slot"], wts.to(dt), dout.to(DEV))
+    dxd, dg, du, dd = moe.moe_experts_backward(d["x_d"], d["offsets"], gdev["gate"], gdev["up"],
+                                               gdev["down"], de)
+    dx = moe.moe_dispatch_backward(dxd, d["row_of_slot"], wl.T, wl.top_k)
+    dl = moe.moe_selected_router_backward(gdev["logits"], idx, dwts, "softmax", True, 1.0)
+    torch.cuda.synchronize()
+
+    name = DT_NAME[dt]
+    st = {k: storage(v) for k, v in inp.items()}
+    l64 = O.to_f64(*st["logits"])
+    ridx, _ = O.route(l64, wl.top_k, True, name)
+    np.testing.assert_array_equal(u32(idx), ridx)
+    _, offsets, tor, ros = O.dispatch(ridx, wl.E)
+    xd = O.gather(O.to_f64(*st["x"]), tor)
+    ry = O.experts(xd, offsets, st["gate"][0], st["up"][0], st["down"][0], name)
+    rw = O.selected_router_weights(l64, ridx, "softmax", True, 1.0)
+    rde, rdw = O.combine_backward(ry, ros, rw, O.to_f64(*storage(dout)))
+    rdxd, rdg, rdu, rdd = O.experts_backward(xd, offsets, st["gate"][0], st["up"][0],
+                                             st["down"][0], name, rde)
+    rdx = O.dispatch_backward(rdxd, ros, wl.T, wl.top_k)
+    rdl = O.selected_router_backward(l64, ridx, rdw, "softmax", True, 1.0)
+    tol = layer_tol(dt)
+    assert rel_max_err(f64(dx), rdx) <= tol
+    assert rel_max_err(f64(dl), rdl) <= tol
+    for got, ref in ((dg, rdg), (du, rdu), (dd, rdd)):
+        assert rel_max_err(f64(got), ref) <= tol
