@@ -61,6 +61,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward chain (combine, experts, dispatch, router) instead")
     return ap.parse_args()
 
 
@@ -339,6 +341,66 @@ def run_route_only(args):
     print(json.dumps(line), flush=True)
 
 
+def run_backward(args):
+    """The backward chain on a layer workload: combine_backward -> experts backward ->
+    dispatch_backward -> router backward, inputs from one forward, resident in HBM."""
+    import mixture_experts_routing_moe_gb300 as moe
+    from mixture_experts_routing_moe_gb300 import build as build_mod
+    build_mod.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]
+    inp = W.make_layer_inputs(wl, dev)
+    x, logits, gate, up, down = (inp[k] for k in ("x", "logits", "gate", "up", "down"))
+    idx, _ = moe.moe_route(logits, wl.top_k, wl.renormalize)
+    d = moe.moe_dispatch(x, idx, wl.E)
+    y = moe.moe_experts_forward_dispatched(d["x_d"], d["offsets"], gate, up, down)
+    wts = moe.moe_selected_router_weights(logits, idx, "softmax", wl.renormalize, 1.0).to(x.dtype)
+    dout = torch.randn(wl.T, wl.H, device=dev, generator=torch.Generator(device=dev).manual_seed(1)).to(x.dtype)
+    R = wl.T * wl.top_k
+    ws = torch.empty(moe.binding.lib().moe_experts_backward_workspace_bytes(R, wl.I),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        de, dw = moe.moe_combine_backward(y, d["row_of_slot"], wts, dout)
+        if ev: ev[1].record(stream)
+        dxd, dg, du, dd = moe.moe_experts_backward(d["x_d"], d["offsets"], gate, up, down, de, ws=ws)
+        if ev: ev[2].record(stream)
+        moe.moe_dispatch_backward(dxd, d["row_of_slot"], wl.T, wl.top_k)
+        moe.moe_selected_router_backward(logits, idx, dw, "softmax", wl.renormalize, 1.0)
+        if ev: ev[3].record(stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    tot = float(np.mean([e[0].elapsed_time(e[3]) for e in evs]))
+    exp_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    flops = 16 * R * wl.H * wl.I          # recompute g, u (4) + da (2) + dinput (4) + weight grads (6)
+    # FP32 CUDA-core peak from unit counts and clock: SMs x 128 FMA/clk x 2 x max SM clock
+    props = torch.cuda.get_device_properties(dev)
+    peak = props.multi_processor_count * 128 * 2 * 2.07e9 / 1e12
+    achieved = flops / (exp_ms / 1e3) / 1e12
+    line = {"metric": "MoE backward tokens/s (combine, experts, dispatch, router backward)",
+            "value": wl.T / (tot / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tot, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                       "top_k": wl.top_k},
+            "roofline": {"kernel": "experts backward (FP32 CUDA-core ragged GEMMs)",
+                         "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak,
+                         "peak_source": "derived: SMs x 128 FP32 FMA/clk x 2 x 2.07 GHz",
+                         "traffic": None, "algorithmic_flops_per_launch": flops},
+            "stages_ms": {"experts_backward": exp_ms, "total": tot},
+            "gpu_launches": 10 * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args):
     import mixture_experts_routing_moe_gb300 as moe
     from mixture_experts_routing_moe_gb300 import build as build_mod
@@ -484,6 +546,8 @@ def main():
         run_reference(args)
     elif W.WORKLOADS[args.workload].H == 0:
         run_route_only(args)
+    elif args.backward:
+        run_backward(args)
     else:
         run_ours(args)
 
