@@ -445,10 +445,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ================================================================ CTA-pair kernels
 // A cluster of two CTAs on neighbouring SMs computes one 256 x 256 tile with cta_group::2 MMAs:
 // CTA r loads rows [128 r, 128 r + 128) of the tile's A rows and the r-th 128-row half of its B
-// rows (gate/up: r = 0 gate, r = 1 up; down: the two halves of the 256 output columns).  One
-// thread of CTA 0 issues tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16); the MMA reads both
-// CTAs' shared memory at the same offsets and leaves each CTA's 128 accumulator rows in that
-// CTA's TMEM.  With half of B per CTA a stage is 32 KB, so six stages fit, and each CTA pulls a
+// rows.  For gate/up the B halves interleave the two projections: CTA r holds gate rows and up
+// rows [64 r, 64 r + 64) of the 128 intermediate columns, so accumulator columns 0-63 / 64-127
+// are gate / up of one 64-column group and 128-191 / 192-255 gate / up of the other.  For down
+// the halves are the two halves of the 256 output columns.  One thread of CTA 0 issues
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16); the MMA reads both CTAs' shared memory
+// at the same offsets and leaves each CTA's 128 accumulator rows in that CTA's TMEM.
+// An expert's last tile with at most 128 rows runs as M = 128 (64 rows per CTA): each CTA's TMEM
+// lanes 0-63 then hold its 64 rows for N columns 0-127 and lanes 64-127 the same rows for N
+// columns 128-255, in TMEM columns 0-127 (layout measured on GB300).  This keeps the padding of
+// ragged experts at 128-row granularity.  With half of B per CTA a stage is 32 KB, so six stages fit, and each CTA pulls a
 // third fewer bytes per FLOP through L2 than a single-CTA 128 x 256 tile.
 // Synchronisation: both CTAs' TMA loads signal CTA 0's full barrier (CTA 0 arms it for both);
 // CTA 0's MMA commits are multicast to the empty / tmem-full barriers of both CTAs; all eight
@@ -583,13 +589,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool stop = false;
       const uint64_t keep = policy_evict_last(), other = policy_evict_normal();
-      const CUtensorMap* mapB = (GATEUP && !leader) ? &mapB1 : &mapB0;
       for (int t = pair; t < total && !stop; t += npairs) {
         int e, m, n;
         const bool a_res = decode_tile<BM2>(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
         const uint64_t pa = a_res ? keep : other, pb = a_res ? other : keep;
-        const int a_row = __ldg(p.offsets + e) + m * BM2 + (int)rank * 128;
-        const int b_row = GATEUP ? e * p.b_rows + n * (BN / 2)
+        const int r0 = __ldg(p.offsets + e) + m * BM2;
+        const bool half = __ldg(p.offsets + e + 1) - r0 <= 128;
+        const int a_row = r0 + (int)rank * (half ? 64 : 128);
+        const int b_row = GATEUP ? e * p.b_rows + n * (BN / 2) + (int)rank * 64
                                  : e * p.b_rows + n * BN + (int)rank * 128;
         for (int kb = 0; kb < p.KB; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_f, p.status)) {
@@ -600,7 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = map_to_rank(full_bar(stage), 0);
           if (leader) mbar_expect_tx(full_bar(stage), 2 * STAGE2_BYTES);
           tma_load_2d_pair(sa, &mapA, fb, kb * BK, a_row, pa);
-          tma_load_2d_pair(sb, mapB, fb, kb * BK, b_row, pb);
+          if (GATEUP) {  // 64 gate rows, then the same 64 up rows
+            tma_load_2d_pair(sb, &mapB0, fb, kb * BK, b_row, pb);
+            tma_load_2d_pair(sb + B2_BYTES / 2, &mapB1, fb, kb * BK, b_row, pb);
+          } else {
+            tma_load_2d_pair(sb, &mapB0, fb, kb * BK, b_row, pb);
+          }
           ++armed;
           if (++stage == STAGES2) {
             stage = 0;
@@ -623,11 +635,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (leader && lane == 0) {
       // ------------------------------------------------------------ MMA issuer (CTA 0 only)
-      constexpr uint32_t idesc = make_idesc(BF16, BM2, BN);
+      constexpr uint32_t idesc_full = make_idesc(BF16, BM2, BN);
+      constexpr uint32_t idesc_half = make_idesc(BF16, BM2 / 2, BN);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool stop = false;
       for (int t = pair; t < total && !stop; t += npairs) {
+        int e, m, n;
+        decode_tile<BM2>(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
+        const int r0 = __ldg(p.offsets + e) + m * BM2;
+        const uint32_t idesc = __ldg(p.offsets + e + 1) - r0 <= 128 ? idesc_half : idesc_full;
         if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_f, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -667,18 +684,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_f, p.status);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
-      const int row = __ldg(p.offsets + e) + m * BM2 + (int)rank * 128 + q * 32 + lane;
-      const bool valid = row < __ldg(p.offsets + e + 1);
+      const int r0 = __ldg(p.offsets + e) + m * BM2;
+      const int r_end = __ldg(p.offsets + e + 1);
+      const bool half = r_end - r0 <= 128;
+      // full tile: lane quarter q holds rows 128 rank + 32 q + lane over all N columns;
+      // half tile: quarters 0-1 hold rows 64 rank + 32 q + lane for N columns 0-127, quarters 2-3
+      // the same rows for N columns 128-255 (TMEM columns 0-127 in both cases)
+      const int row =
+          r0 + (half ? (int)rank * 64 + (q & 1) * 32 + lane : (int)rank * 128 + q * 32 + lane);
+      const int nhalf = half ? (q >> 1) : 0;  // which half of N this warp holds (half tiles)
+      const bool valid = row < r_end;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       uint8_t* orow = p.out + (size_t)row * p.N * 2;
       if (GATEUP) {
+        // output column group j (32 columns): gate at accumulator column gc, up at gc + 64;
+        // full tile: j = 0..3, gc = (j & 1) * 32 + (j >> 1) * 128, outputs n*128 + 32 j;
+        // half tile: j = 0..1, gc = 32 j, outputs n*128 + 64 nhalf + 32 j
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int j = 0; j < (half ? 2 : 4); ++j) {
+          const int gc = half ? 32 * j : (j & 1) * 32 + (j >> 1) * 128;
           uint32_t g[32], u[32];
-          tmem_ld32(taddr + c * 32, g);
-          tmem_ld32(taddr + BN / 2 + c * 32, u);
+          tmem_ld32(taddr + gc, g);
+          tmem_ld32(taddr + gc + 64, u);
           tmem_wait_ld();
-          const int col0 = n * (BN / 2) + c * 32;
+          const int col0 = n * (BN / 2) + (half ? 64 * nhalf + 32 * j : 32 * j);
           if (valid) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -702,11 +731,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < (half ? 4 : 8); ++c) {
           uint32_t r[32];
           tmem_ld32(taddr + c * 32, r);
           tmem_wait_ld();
-          const int col0 = n * BN + c * 32;
+          const int col0 = n * BN + 128 * nhalf + c * 32;
           if (valid) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -840,6 +869,11 @@ cudaError_t launch_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, c
     return cudaErrorInvalidValue;
 
   TcParams p1{offsets, (uint8_t*)a, status, E, I, (H + BK - 1) / BK, (I + BN / 2 - 1) / (BN / 2), I};
+  if (pair) {  // the pair kernel loads gate and up in 64-row boxes (interleaved B halves)
+    if (!make_map(&mg, gate, BF16, H, (int64_t)E * I, BN / 4) ||
+        !make_map(&mu, up, BF16, H, (int64_t)E * I, BN / 4))
+      return cudaErrorInvalidValue;
+  }
   err = pair ? launch_pair<true, BF16>(mx, mg, mu, p1, rows, dev, s)
              : launch_one<true, BF16>(mx, mg, mu, p1, rows, sms, s);
   if (err != cudaSuccess) return err;
