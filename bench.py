@@ -38,7 +38,10 @@ from mixture_experts_routing_moe_gb300 import workloads as W  # noqa: E402
 METRIC = "MoE fwd tokens/s; grouped-GEMM TFLOP/s vs bf16 peak; route/combine GB/s vs HBM"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS_PER_FORWARD = 8   # route 1, dispatch 4 (count, scan, scatter, rows), experts 2, combine 1
+def kernels_per_forward(wl) -> int:
+    """route 1 + dispatch (2 for <= 4096 slots: fused index kernel + rows; else 4) + experts 2
+    + combine 1."""
+    return 1 + (2 if wl.T * wl.top_k <= 4096 else 4) + 2 + 1
 STAGES = ["route", "dispatch", "gate_up_gemm", "down_gemm", "combine"]
 # DRAM traffic of one gate/up GEMM launch on the skewed workload, from the ncu capture summarised
 # in profiles/gateup_tc_skewed.md, valid while experts_tc.cu has the recorded hash.
@@ -532,7 +535,7 @@ def run_ours(args):
             "hbm_peak_gbs": pk["hbm_gbs"],
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": KERNELS_PER_FORWARD * args.steps,
+            "gpu_launches": kernels_per_forward(wl) * args.steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

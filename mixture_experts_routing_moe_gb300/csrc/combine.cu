@@ -2,8 +2,9 @@
 //
 // out[t] = sum_{j=0..k-1} w[t, j] * y[row_of_slot[t*k + j]], FP32 accumulation in the fixed slot
 // order j = 0..k-1 (no atomics: the result is the same bits on every run), rounded once to the
-// output dtype.  One warp per token; lane i handles 16-byte column chunks i, i+32, ...  The k
-// (row, weight) pairs of a token are loaded by the lanes once and broadcast with shuffles.
+// output dtype.  A token is spread over ceil(H / (32 * 16-byte chunk)) warps, one 16-byte column
+// chunk per lane, so short batches still fill the GPU; each warp loads the token's k
+// (row, weight) pairs through its lanes and broadcasts them with shuffles.
 #include "common.cuh"
 #include "launch.h"
 
@@ -16,59 +17,58 @@ template <typename TY, typename TW, bool VEC>
 __global__ void __launch_bounds__(kCombWarps * 32)
     moe_combine_kernel(const TY* __restrict__ y, const uint32_t* __restrict__ row_of_slot,
                        const TW* __restrict__ w, int64_t T, int64_t H, int k,
-                       TY* __restrict__ out) {
+                       int64_t warps_per_token, TY* __restrict__ out) {
   const int lane = threadIdx.x & 31;
-  const int64_t t = (int64_t)blockIdx.x * kCombWarps + (threadIdx.x >> 5);
+  const int64_t gw = (int64_t)blockIdx.x * kCombWarps + (threadIdx.x >> 5);
+  const int64_t t = gw / warps_per_token;
   if (t >= T) return;
   constexpr int VW = VEC ? 16 / (int)sizeof(TY) : 1;
   const int64_t chunks = H / VW;
-  for (int64_t c0 = 0; c0 < chunks; c0 += 32) {
-    const int64_t c = c0 + lane;
-    float acc[VW];
+  const int64_t c = (gw - t * warps_per_token) * 32 + lane;  // this lane's column chunk
+  float acc[VW];
 #pragma unroll
-    for (int i = 0; i < VW; ++i) acc[i] = 0.f;
-    bool poisoned = false;
-    for (int jb = 0; jb < k; jb += 32) {
-      uint32_t my_row = kInvalidRow;
-      float my_w = 0.f;
-      if (jb + lane < k) {
-        my_row = row_of_slot[t * k + jb + lane];
-        my_w = Dt<TW>::to_f(w[t * k + jb + lane]);
+  for (int i = 0; i < VW; ++i) acc[i] = 0.f;
+  bool poisoned = false;
+  for (int jb = 0; jb < k; jb += 32) {
+    uint32_t my_row = kInvalidRow;
+    float my_w = 0.f;
+    if (jb + lane < k) {
+      my_row = row_of_slot[t * k + jb + lane];
+      my_w = Dt<TW>::to_f(w[t * k + jb + lane]);
+    }
+    const int nj = min(32, k - jb);
+    for (int jj = 0; jj < nj; ++jj) {
+      const uint32_t r = __shfl_sync(0xFFFFFFFFu, my_row, jj);
+      const float wj = __shfl_sync(0xFFFFFFFFu, my_w, jj);
+      if (r == kInvalidRow) {
+        poisoned = true;
+        continue;
       }
-      const int nj = min(32, k - jb);
-      for (int jj = 0; jj < nj; ++jj) {
-        const uint32_t r = __shfl_sync(0xFFFFFFFFu, my_row, jj);
-        const float wj = __shfl_sync(0xFFFFFFFFu, my_w, jj);
-        if (r == kInvalidRow) {
-          poisoned = true;
-          continue;
-        }
-        if (c < chunks) {
-          if (VEC) {
-            Vec16<TY> q;
-            q.u = ld_nc_v4(y + (int64_t)r * H + c * VW);
-            float f[VW];
-            q.to_float(f);
+      if (c < chunks) {
+        if (VEC) {
+          Vec16<TY> q;
+          q.u = ld_nc_v4(y + (int64_t)r * H + c * VW);
+          float f[VW];
+          q.to_float(f);
 #pragma unroll
-            for (int i = 0; i < VW; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
-          } else {
-            acc[0] = fmaf(wj, Dt<TY>::to_f(y[(int64_t)r * H + c]), acc[0]);
-          }
+          for (int i = 0; i < VW; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+        } else {
+          acc[0] = fmaf(wj, Dt<TY>::to_f(y[(int64_t)r * H + c]), acc[0]);
         }
       }
     }
-    if (c < chunks) {
-      if (poisoned) {
+  }
+  if (c < chunks) {
+    if (poisoned) {
 #pragma unroll
-        for (int i = 0; i < VW; ++i) acc[i] = __int_as_float(0x7FC00000);
-      }
-      if (VEC) {
-        Vec16<TY> q;
-        q.from_float(acc);
-        st_v4(out + t * H + c * VW, q.u);
-      } else {
-        out[t * H + c] = Dt<TY>::from_f(acc[0]);
-      }
+      for (int i = 0; i < VW; ++i) acc[i] = __int_as_float(0x7FC00000);
+    }
+    if (VEC) {
+      Vec16<TY> q;
+      q.from_float(acc);
+      st_v4(out + t * H + c * VW, q.u);
+    } else {
+      out[t * H + c] = Dt<TY>::from_f(acc[0]);
     }
   }
 }
@@ -78,13 +78,15 @@ cudaError_t launch_combine_t(const void* y, const uint32_t* ros, const void* w, 
                              int64_t H, int k, void* out, cudaStream_t s) {
   const bool vec = ((uintptr_t)y % 16 == 0) && ((uintptr_t)out % 16 == 0) &&
                    ((H * (int64_t)sizeof(TY)) % 16 == 0);
-  const unsigned blocks = (unsigned)((T + kCombWarps - 1) / kCombWarps);
+  const int64_t chunks = vec ? H * (int64_t)sizeof(TY) / 16 : H;
+  const int64_t wpt = (chunks + 31) / 32;  // warps per token: one column chunk per lane
+  const unsigned blocks = (unsigned)((T * wpt + kCombWarps - 1) / kCombWarps);
   if (vec)
     moe_combine_kernel<TY, TW, true><<<blocks, kCombWarps * 32, 0, s>>>(
-        (const TY*)y, ros, (const TW*)w, T, H, k, (TY*)out);
+        (const TY*)y, ros, (const TW*)w, T, H, k, wpt, (TY*)out);
   else
     moe_combine_kernel<TY, TW, false><<<blocks, kCombWarps * 32, 0, s>>>(
-        (const TY*)y, ros, (const TW*)w, T, H, k, (TY*)out);
+        (const TY*)y, ros, (const TW*)w, T, H, k, wpt, (TY*)out);
   return cudaGetLastError();
 }
 

@@ -14,6 +14,7 @@
 //                last term from match.any ranks.  Writes row_of_slot and token_of_row.
 //   4. rows    — one block per token reads x[t] once (16-byte loads) and writes it to the k rows
 //                row_of_slot[t*k + 0..k-1] of x_d.
+// Batches of at most 4096 slots run steps 1-3 in one block with the histograms in shared memory.
 // Expert ids >= E are not dispatched: their row_of_slot is 0xFFFFFFFF and the status word gets
 // the index bit.  No access goes out of bounds for any id value.
 #include <mutex>
@@ -155,6 +156,92 @@ __global__ void __launch_bounds__(kDispWarps * 32)
   }
 }
 
+// Short batches (R <= kSmallR slots): count, scan and scatter in one block of kSmallWarps warps,
+// histograms in shared memory; the same stable order as the three-kernel path (warp w owns the
+// contiguous chunk [w*CH, w*CH + CH) and ranks inside a chunk come from match.any).
+constexpr int kSmallWarps = 8;
+constexpr int64_t kSmallR = 4096;
+__global__ void __launch_bounds__(kSmallWarps * 32)
+    moe_dispatch_small(const uint32_t* __restrict__ idx, int64_t R, int E, int k, int CH,
+                       int32_t* __restrict__ offsets, uint32_t* __restrict__ token_of_row,
+                       uint32_t* __restrict__ row_of_slot, unsigned* status) {
+  extern __shared__ int32_t small_smem[];
+  int32_t* hist = small_smem;                         // [kSmallWarps][E]
+  int32_t* off = small_smem + kSmallWarps * E;        // [E + 1]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int64_t s0 = (int64_t)warp * CH, s1 = (R < s0 + CH) ? R : s0 + CH;
+  int32_t* h = hist + warp * E;
+  bool bad = false;
+  for (int64_t base = s0; base < s1; base += 32) {
+    const int64_t s = base + lane;
+    const bool act = s < s1;
+    const uint32_t e = act ? idx[s] : 0xFFFFFFFFu;
+    const bool valid = act && e < (uint32_t)E;
+    bad |= act && !valid;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : 0xFFFFFFFFu);
+    if (valid && lane == __ffs(peers) - 1) h[e] += __popc(peers);
+    __syncwarp();
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(status, kStatusIndex);
+  __syncthreads();
+  // per expert: exclusive prefix over the chunks, and the expert's total
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t run = 0;
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const int32_t c = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += c;
+    }
+    off[e] = run;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the totals -> offsets
+    int32_t carry = 0;
+    for (int b = 0; b < E; b += 32) {
+      const int e = b + lane;
+      const int32_t c = e < E ? off[e] : 0;
+      int32_t x = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (e < E) {
+        off[e] = carry + x - c;
+        offsets[e] = carry + x - c;
+      }
+      carry += __shfl_sync(0xFFFFFFFFu, x, 31);
+    }
+    if (lane == 0) {
+      off[E] = carry;
+      offsets[E] = carry;
+    }
+  }
+  __syncthreads();
+  for (int e = lane; e < E; e += 32) h[e] += off[e];  // running row of each expert in this chunk
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int64_t base = s0; base < s1; base += 32) {
+    const int64_t s = base + lane;
+    const bool act = s < s1;
+    const uint32_t e = act ? idx[s] : 0xFFFFFFFFu;
+    const bool valid = act && e < (uint32_t)E;
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : 0xFFFFFFFFu);
+    if (valid) {
+      const uint32_t row = (uint32_t)(h[e] + __popc(peers & lt));
+      row_of_slot[s] = row;
+      token_of_row[row] = (uint32_t)(s / k);
+    } else if (act) {
+      row_of_slot[s] = kInvalidRow;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) h[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
 // One block per token (grid-stride): x[t] is read once and written to its k dispatched rows.
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS)
@@ -222,14 +309,21 @@ cudaError_t launch_dispatch(const void* x, int xdt, int64_t T, int64_t H, const 
                             uint32_t* row_of_slot, int32_t* hist, unsigned* status,
                             cudaStream_t s) {
   const int64_t R = T * k;
-  const DispatchPlan p = dispatch_plan(R);
-  const size_t smem = (size_t)kDispWarps * E * sizeof(int32_t);
-  const unsigned blocks = (unsigned)((p.W + kDispWarps - 1) / kDispWarps);
-  moe_dispatch_count<<<blocks, kDispWarps * 32, smem, s>>>(idx, R, E, p.W, p.CH, hist, status);
-  int32_t* totals = hist + (size_t)p.W * E;
-  moe_dispatch_scan<<<E, kScanThreads, 0, s>>>(hist, p.W, E, totals);
-  moe_dispatch_scatter<<<blocks, kDispWarps * 32, smem, s>>>(
-      idx, R, E, k, p.W, p.CH, hist, totals, offsets, token_of_row, row_of_slot);
+  if (R <= kSmallR) {
+    const int CH = (int)(((R + kSmallWarps - 1) / kSmallWarps + 31) / 32 * 32);
+    const size_t smem = ((size_t)kSmallWarps * E + E + 1) * sizeof(int32_t);
+    moe_dispatch_small<<<1, kSmallWarps * 32, smem, s>>>(idx, R, E, k, CH, offsets, token_of_row,
+                                                         row_of_slot, status);
+  } else {
+    const DispatchPlan p = dispatch_plan(R);
+    const size_t smem = (size_t)kDispWarps * E * sizeof(int32_t);
+    const unsigned blocks = (unsigned)((p.W + kDispWarps - 1) / kDispWarps);
+    moe_dispatch_count<<<blocks, kDispWarps * 32, smem, s>>>(idx, R, E, p.W, p.CH, hist, status);
+    int32_t* totals = hist + (size_t)p.W * E;
+    moe_dispatch_scan<<<E, kScanThreads, 0, s>>>(hist, p.W, E, totals);
+    moe_dispatch_scatter<<<blocks, kDispWarps * 32, smem, s>>>(
+        idx, R, E, k, p.W, p.CH, hist, totals, offsets, token_of_row, row_of_slot);
+  }
   const size_t esz = xdt == MOE_F32 ? 4 : 2;
   const int64_t vecs = H * (int64_t)esz / 16;
   int64_t grid = T < 65536 ? T : 65536;

@@ -91,9 +91,10 @@ def _expected_dispatch(idx_np, E):
 
 @pytest.mark.parametrize("case", ["uniform", "zipf", "one_expert", "many_empty", "invalid_ids",
                                   "large"])
-def test_dispatch_matches_oracle(case):
+@pytest.mark.parametrize("T0", [1500, 300])   # 6000 slots: multi-block path; 1200: one block
+def test_dispatch_matches_oracle(case, T0):
     rng = np.random.default_rng(abs(hash(case)) % 2**32)
-    T, E, k, H = 1500, 64, 4, 96
+    T, E, k, H = T0, 64, 4, 96
     if case == "uniform":
         idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
     elif case == "zipf":
