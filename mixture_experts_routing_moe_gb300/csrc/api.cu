@@ -379,7 +379,9 @@ int moe_combine_backward(const void* y, int ydt, const uint32_t* row_of_slot, co
 
 size_t moe_experts_backward_workspace_bytes(int64_t rows, int64_t I) {
   if (rows < 0 || rows >= kMaxRows || I < 1) return 0;
-  return align_up(kWsHeader, 256) + align_up(experts_backward_scratch_bytes(rows, I), 256);
+  const size_t simt = experts_backward_scratch_bytes(rows, I);
+  const size_t tc = experts_backward_tc_scratch_bytes(rows, I);
+  return align_up(kWsHeader, 256) + align_up(simt > tc ? simt : tc, 256);
 }
 
 int moe_experts_backward(const void* x_d, const int32_t* offsets, int64_t rows, const void* gate,
@@ -402,6 +404,15 @@ int moe_experts_backward(const void* x_d, const int32_t* offsets, int64_t rows, 
     return MOE_OK;
   }
   float* scratch = (float*)((uint8_t*)ws + align_up(kWsHeader, 256));
+  unsigned* status = (unsigned*)ws;
+  if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (wdt != MOE_F32 && I % 64 == 0) {
+    const void* ptrs[8] = {x_d, gate, up, down, dy, dinput, dgate, ddown};
+    if (check_tc_align(H, I, ptrs, 8) == MOE_OK && aligned16(dup))
+      return cuda_status(launch_experts_backward_tc(x_d, offsets, rows, gate, up, down, wdt,
+                                                    (int)E, (int)H, (int)I, dy, dinput, dgate,
+                                                    dup, ddown, scratch, status, s));
+  }
   return cuda_status(launch_experts_backward(x_d, offsets, rows, gate, up, down, wdt, (int)E,
                                              (int)H, (int)I, dy, dinput, dgate, dup, ddown,
                                              scratch, s));

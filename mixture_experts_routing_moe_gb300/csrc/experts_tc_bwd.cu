@@ -1,0 +1,503 @@
+// Expert backward on 5th-generation tensor cores for bf16 / f16 layers (ruDNN user guide, §12
+// "MoE-Training erster Ordnung", cache.backward(dexpert)).  Per expert e and its dispatched rows:
+//   DA    da  = dy down_e                       (FP32 [rows, I]; down_e read N-major)
+//   GU    g, u = x gate_e^T, x up_e^T recomputed; epilogue with da:
+//           s = sigmoid(g), dg = da u s (1 + g (1 - s)), du = da g s, a = g s u
+//           -> dgdu [rows, 2I] (dg | du) and a [rows, I], both in the layer dtype
+//   DIN   dinput = [dg du] [gate_e; up_e]       (layer dtype [rows, H]; K = 2I, B read N-major)
+//   WG    dgate_e = dg^T x, dup_e = du^T x, ddown_e = dy^T a   (FP32; both operands M/N-major,
+//         the contraction runs over the expert's rows)
+// One persistent CTA per SM, the warp roles of the forward kernel (TMA producer, MMA issuer,
+// four epilogue warps), 128 x 256 tiles, 4 x 48 KB stages, FP32 accumulators in TMEM.  An
+// operand whose contiguous dimension is M or N is loaded as 64-column boxes and described as an
+// MN-major 128-byte-swizzled matrix (boxes 8 KB apart, 8-row groups 1 KB apart).  In WG the last
+// 64-row K block of an expert would run into the next expert's rows: the MMA warp zeroes those
+// rows in shared memory before the MMAs read them.  All waits are bounded as in the forward.
+#include <type_traits>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tcgen05.cuh"
+#include "tiles.cuh"
+
+namespace moe {
+namespace {
+using namespace tc;
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BOX_BYTES = 64 * 128;  // one 64-row x 64-column box
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxExperts = 1024;
+constexpr size_t kSmemBytes =
+    1024 + (size_t)STAGES * STAGE_BYTES + 256 + (kMaxExperts + 4) * sizeof(int);
+
+enum Mode { DA = 0, GU = 1, DIN = 2, WG = 3 };
+
+// MN-major 128-byte-swizzled operand: 64-column boxes BOX_BYTES apart, 8-row groups 1 KB apart.
+__device__ __forceinline__ uint64_t make_sdesc_mn(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(BOX_BYTES >> 4) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// kind::f16 instruction descriptor with operand majors (bit 15: A MN-major, bit 16: B MN-major)
+__host__ __device__ constexpr uint32_t idesc_majors(bool bf16, int M, int N, bool a_mn, bool b_mn) {
+  return make_idesc(bf16, M, N) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
+}
+
+struct BwdParams {
+  const int32_t* offsets;
+  int E, H, I;
+  int KB;           // K blocks (DA: H/64, GU: H/64, DIN: 2I/64); WG: per expert
+  int NT, MT;       // n-tiles per expert (and m-tiles per expert in WG)
+  int M, N;         // WG: output matrix of each expert is M x N
+  int a_col0;       // WG: first column of A inside its source matrix (du starts at I)
+  const float* da;  // GU: da [rows, I] FP32
+  void* out0;       // DA: da FP32; GU: dgdu; DIN: dinput; WG: C [E, M, N] FP32
+  void* out1;       // GU: a
+  unsigned* status;
+};
+
+template <int MODE>
+__device__ __forceinline__ void decode(int t, const int* pref, const BwdParams& p, int& e, int& m,
+                                       int& n) {
+  if (MODE == WG) {
+    const int per = p.MT * p.NT;
+    e = t / per;
+    const int r = t - e * per;
+    m = r / p.NT;
+    n = r - m * p.NT;
+  } else {  // expert rows in 128-row tiles, n inner: CTAs in flight share an A tile
+    const int j = t / p.NT;
+    e = find_expert(pref, p.E, j);
+    m = j - pref[e];
+    n = t - j * p.NT;
+  }
+}
+
+template <int MODE, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    moe_experts_bwd_tc(const __grid_constant__ CUtensorMap mapA,
+                       const __grid_constant__ CUtensorMap mapB0,
+                       const __grid_constant__ CUtensorMap mapB1, const BwdParams p) {
+  using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr bool A_MN = MODE == WG, B_MN = MODE != GU;
+  extern __shared__ uint8_t tcb_smem_raw[];
+  const uint32_t raw = smem_u32(tcb_smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = tcb_smem_raw + (base - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_f = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* pref = reinterpret_cast<int*>(tmem_slot + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_f = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  if (warp == 2 && MODE != WG) build_mtile_prefix(p.offsets, p.E, BM, pref, lane);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&mapA);
+    tma_prefetch(&mapB0);
+    tma_prefetch(&mapB1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = MODE == WG ? p.E * p.MT * p.NT : pref[p.E] * p.NT;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int stage = 0, armed = 0;
+      uint32_t phase = 0;
+      bool stop = false;
+      const uint64_t pol = policy_evict_normal();
+      for (int t = blockIdx.x; t < total && !stop; t += gridDim.x) {
+        int e, m, n;
+        decode<MODE>(t, pref, p, e, m, n);
+        const int r0 = __ldg(p.offsets + e), r1 = __ldg(p.offsets + e + 1);
+        const int KB = MODE == WG ? (r1 - r0 + BK - 1) / BK : p.KB;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_f, p.status)) {
+            stop = true;
+            break;
+          }
+          const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+          mbar_expect_tx(full_bar(stage), STAGE_BYTES);
+          if (MODE == WG) {  // A: rows r0 + 64 kb, columns a_col0 + 128 m (two 64-column boxes)
+            const int y = r0 + kb * BK;
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d(sa + j * BOX_BYTES, &mapA, full_bar(stage), p.a_col0 + m * BM + 64 * j, y, pol);
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(sb + j * BOX_BYTES, &mapB0, full_bar(stage), n * BN + 64 * j, y, pol);
+          } else {
+            tma_load_2d(sa, &mapA, full_bar(stage), kb * BK, r0 + m * BM, pol);
+            if (MODE == GU) {  // K-major: 128 gate rows then the same 128 up rows
+              const int br = e * p.I + n * (BN / 2);
+              tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, br, pol);
+              tma_load_2d(sb + B_BYTES / 2, &mapB1, full_bar(stage), kb * BK, br, pol);
+            } else {
+              // N-major B: rows are K.  DA: down [E*H, I];  DIN: gate (k < I) / up (k >= I)
+              const CUtensorMap* mb = &mapB0;
+              int kr;
+              if (MODE == DA) {
+                kr = e * p.H + kb * BK;
+              } else {
+                const int k0 = kb * BK;
+                if (k0 >= p.I) mb = &mapB1;
+                kr = e * p.I + (k0 >= p.I ? k0 - p.I : k0);
+              }
+              for (int j = 0; j < 4; ++j)
+                tma_load_2d(sb + j * BOX_BYTES, mb, full_bar(stage), n * BN + 64 * j, kr, pol);
+            }
+          }
+          ++armed;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (*abort_f) {
+        for (int i = 0; i < min(armed, STAGES); ++i) {
+          if (stage == 0) {
+            stage = STAGES - 1;
+            phase ^= 1u;
+          } else {
+            --stage;
+          }
+          wait_drain(full_bar(stage), phase);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA warp (lane 0 issues)
+    constexpr uint32_t idesc = idesc_majors(BF16, BM, BN, A_MN, B_MN);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool stop = false;
+    for (int t = blockIdx.x; t < total && !stop; t += gridDim.x) {
+      int e, m, n;
+      decode<MODE>(t, pref, p, e, m, n);
+      const int r0 = __ldg(p.offsets + e), r1 = __ldg(p.offsets + e + 1);
+      const int KB = MODE == WG ? (r1 - r0 + BK - 1) / BK : p.KB;
+      bool ok = lane != 0 || wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_f, p.status);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < KB; ++kb) {
+        ok = wait_bounded(full_bar(stage), phase, abort_f, p.status);
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+          stop = true;
+          break;
+        }
+        const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+        if (MODE == WG) {
+          const int valid = r1 - (r0 + kb * BK);
+          if (valid < BK) {  // rows past the expert's end belong to the next expert: zero them
+            const int nz = (BK - valid) * 6 * 8;  // rows x (2 A + 4 B boxes) x 8 chunks
+            uint8_t* g0 = gbase + stage * STAGE_BYTES;
+            for (int i = lane; i < nz; i += 32) {
+              const int row = valid + i / 48, rem = i % 48, box = rem / 8, ch = rem % 8;
+              uint8_t* dst = g0 + (box < 2 ? box * BOX_BYTES : A_BYTES + (box - 2) * BOX_BYTES) +
+                             row * 128 + ch * 16;
+              *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint64_t da = A_MN ? make_sdesc_mn(sa) : make_sdesc(sa);
+          const uint64_t db = B_MN ? make_sdesc_mn(sb) : make_sdesc(sb);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)  // 16 K: 32 bytes (K-major) or 2 KB (MN-major)
+            umma_f16(d_tmem, da + (A_MN ? 128u : 2u) * kk, db + (B_MN ? 128u : 2u) * kk, idesc,
+                     (kb | kk) != 0);
+          umma_commit(empty_bar(stage));
+        }
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (stop) break;
+      if (lane == 0) umma_commit(tfull_bar(acc));
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) {
+      umma_commit(drain_bar);
+      wait_drain(drain_bar, 0);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (warps 2..5)
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int e, m, n;
+      decode<MODE>(t, pref, p, e, m, n);
+      const bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_f, p.status);
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      tc_fence_after();
+      const int r0 = __ldg(p.offsets + e), r1 = __ldg(p.offsets + e + 1);
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      if (MODE == WG) {
+        const int mrow = m * BM + q * 32 + lane;  // output row of C_e
+        const bool empty = r1 == r0;              // no rows: the gradient is zero
+        float* crow = reinterpret_cast<float*>(p.out0) + ((size_t)e * p.M + mrow) * p.N;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c * 32, r);
+          tmem_wait_ld();
+          const int col0 = n * BN + c * 32;
+          if (mrow < p.M) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              if (col0 + v * 4 < p.N)
+                st_v4(crow + col0 + v * 4,
+                      empty ? make_uint4(0, 0, 0, 0)
+                            : make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]));
+          }
+        }
+      } else {
+        const int row = r0 + m * BM + q * 32 + lane;
+        const bool valid = row < r1;
+        if (MODE == GU) {
+          const float* darow = p.da + (size_t)row * p.I;
+          T* dg_row = reinterpret_cast<T*>(p.out0) + (size_t)row * 2 * p.I;
+          T* a_row = reinterpret_cast<T*>(p.out1) + (size_t)row * p.I;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t g[32], u[32];
+            tmem_ld32(taddr + c * 32, g);
+            tmem_ld32(taddr + BN / 2 + c * 32, u);
+            tmem_wait_ld();
+            const int col0 = n * (BN / 2) + c * 32;
+            if (valid) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                if (col0 + v * 8 < p.I) {
+                  float dv[8];
+                  *reinterpret_cast<float4*>(dv) = *reinterpret_cast<const float4*>(darow + col0 + v * 8);
+                  *reinterpret_cast<float4*>(dv + 4) = *reinterpret_cast<const float4*>(darow + col0 + v * 8 + 4);
+                  uint32_t pg[4], pu[4], pa[4];
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    float dgv[2], duv[2], av[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                      const float gv = __uint_as_float(g[v * 8 + i * 2 + h]);
+                      const float uv = __uint_as_float(u[v * 8 + i * 2 + h]);
+                      const float sg = 1.f / (1.f + __expf(-gv));
+                      const float act = gv * sg, d = dv[i * 2 + h];
+                      dgv[h] = d * uv * sg * (1.f + gv * (1.f - sg));
+                      duv[h] = d * act;
+                      av[h] = act * uv;
+                    }
+                    pg[i] = pack2<BF16>(dgv[0], dgv[1]);
+                    pu[i] = pack2<BF16>(duv[0], duv[1]);
+                    pa[i] = pack2<BF16>(av[0], av[1]);
+                  }
+                  st_v4(dg_row + col0 + v * 8, make_uint4(pg[0], pg[1], pg[2], pg[3]));
+                  st_v4(dg_row + p.I + col0 + v * 8, make_uint4(pu[0], pu[1], pu[2], pu[3]));
+                  st_v4(a_row + col0 + v * 8, make_uint4(pa[0], pa[1], pa[2], pa[3]));
+                }
+              }
+            }
+          }
+        } else {  // DA (FP32 out, N = I) or DIN (layer dtype out, N = H)
+          const int Nout = MODE == DA ? p.I : p.H;
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            uint32_t r[32];
+            tmem_ld32(taddr + c * 32, r);
+            tmem_wait_ld();
+            const int col0 = n * BN + c * 32;
+            if (valid) {
+              if (MODE == DA) {
+                float* o = reinterpret_cast<float*>(p.out0) + (size_t)row * Nout;
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                  if (col0 + v * 4 < Nout)
+                    st_v4(o + col0 + v * 4, make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]));
+              } else {
+                T* o = reinterpret_cast<T*>(p.out0) + (size_t)row * Nout;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  if (col0 + v * 8 < Nout) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                      pk[i] = pack2<BF16>(__uint_as_float(r[v * 8 + i * 2]),
+                                          __uint_as_float(r[v * 8 + i * 2 + 1]));
+                    st_v4(o + col0 + v * 8, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int MODE, bool BF16>
+cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                        const BwdParams& p, int64_t upper_tiles, int sms, cudaStream_t s) {
+  auto kern = moe_experts_bwd_tc<MODE, BF16>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const int grid = (int)(upper_tiles < sms ? upper_tiles : sms);
+  if (grid < 1) return cudaSuccess;
+  kern<<<grid, kThreads, kSmemBytes, s>>>(a, b0, b1, p);
+  return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, const void* gate,
+                     const void* up, const void* down, int E, int H, int I, const void* dy,
+                     void* dinput, float* dgate, float* dup, float* ddown, void* scratch,
+                     unsigned* status, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  // scratch: da FP32 [rows, I] | dgdu [rows, 2I] | a [rows, I] (layer dtype)
+  float* da = (float*)scratch;
+  uint8_t* dgdu = (uint8_t*)scratch + align_up((size_t)rows * I * 4, 256);
+  uint8_t* abuf = dgdu + align_up((size_t)rows * 2 * I * 2, 256);
+  const int64_t mt_upper = (rows + BM - 1) / BM + E;
+  CUtensorMap mA, mB0, mB1;
+  BwdParams p{};
+  p.offsets = offsets;
+  p.E = E;
+  p.H = H;
+  p.I = I;
+  p.status = status;
+
+  // 1. da = dy down_e
+  if (!make_map_2d(&mA, dy, BF16, H, rows, BK, BM) ||
+      !make_map_2d(&mB0, down, BF16, I, (int64_t)E * H, 64, 64))
+    return cudaErrorInvalidValue;
+  p.KB = (H + BK - 1) / BK;
+  p.NT = (I + BN - 1) / BN;
+  p.out0 = da;
+  err = launch_mode<DA, BF16>(mA, mB0, mB0, p, mt_upper * p.NT, sms, s);
+  if (err != cudaSuccess) return err;
+
+  // 2. g, u recomputed; epilogue -> dg | du, a
+  if (!make_map_2d(&mA, x_d, BF16, H, rows, BK, BM) ||
+      !make_map_2d(&mB0, gate, BF16, H, (int64_t)E * I, BK, BN / 2) ||
+      !make_map_2d(&mB1, up, BF16, H, (int64_t)E * I, BK, BN / 2))
+    return cudaErrorInvalidValue;
+  p.KB = (H + BK - 1) / BK;
+  p.NT = (I + BN / 2 - 1) / (BN / 2);
+  p.da = da;
+  p.out0 = dgdu;
+  p.out1 = abuf;
+  err = launch_mode<GU, BF16>(mA, mB0, mB1, p, mt_upper * p.NT, sms, s);
+  if (err != cudaSuccess) return err;
+
+  // 3. dinput = [dg du] [gate_e; up_e]
+  if (!make_map_2d(&mA, dgdu, BF16, 2 * (int64_t)I, rows, BK, BM) ||
+      !make_map_2d(&mB0, gate, BF16, H, (int64_t)E * I, 64, 64) ||
+      !make_map_2d(&mB1, up, BF16, H, (int64_t)E * I, 64, 64))
+    return cudaErrorInvalidValue;
+  p.KB = 2 * I / BK;
+  p.NT = (H + BN - 1) / BN;
+  p.out0 = dinput;
+  err = launch_mode<DIN, BF16>(mA, mB0, mB1, p, mt_upper * p.NT, sms, s);
+  if (err != cudaSuccess) return err;
+
+  // 4. weight gradients, contracted over each expert's rows
+  CUtensorMap mX;
+  if (!make_map_2d(&mA, dgdu, BF16, 2 * (int64_t)I, rows, 64, 64) ||
+      !make_map_2d(&mX, x_d, BF16, H, rows, 64, 64))
+    return cudaErrorInvalidValue;
+  p.M = I;
+  p.N = H;
+  p.MT = (I + BM - 1) / BM;
+  p.NT = (H + BN - 1) / BN;
+  p.out0 = dgate;
+  p.a_col0 = 0;
+  err = launch_mode<WG, BF16>(mA, mX, mX, p, (int64_t)E * p.MT * p.NT, sms, s);
+  if (err != cudaSuccess) return err;
+  p.out0 = dup;
+  p.a_col0 = I;
+  err = launch_mode<WG, BF16>(mA, mX, mX, p, (int64_t)E * p.MT * p.NT, sms, s);
+  if (err != cudaSuccess) return err;
+  CUtensorMap mY, mAct;
+  if (!make_map_2d(&mY, dy, BF16, H, rows, 64, 64) ||
+      !make_map_2d(&mAct, abuf, BF16, I, rows, 64, 64))
+    return cudaErrorInvalidValue;
+  p.M = H;
+  p.N = I;
+  p.MT = (H + BM - 1) / BM;
+  p.NT = (I + BN - 1) / BN;
+  p.out0 = ddown;
+  p.a_col0 = 0;
+  return launch_mode<WG, BF16>(mY, mAct, mAct, p, (int64_t)E * p.MT * p.NT, sms, s);
+}
+
+}  // namespace
+
+size_t experts_backward_tc_scratch_bytes(int64_t rows, int64_t I) {
+  return align_up((size_t)rows * I * 4, 256) + align_up((size_t)rows * 2 * I * 2, 256) +
+         align_up((size_t)rows * I * 2, 256);
+}
+
+cudaError_t launch_experts_backward_tc(const void* x_d, const int32_t* offsets, int64_t rows,
+                                       const void* gate, const void* up, const void* down,
+                                       int wdt, int E, int H, int I, const void* dy, void* dinput,
+                                       float* dgate, float* dup, float* ddown, void* scratch,
+                                       unsigned* status, cudaStream_t s) {
+  if (wdt == MOE_BF16)
+    return bwd_tc_t<true>(x_d, offsets, rows, gate, up, down, E, H, I, dy, dinput, dgate, dup,
+                          ddown, scratch, status, s);
+  if (wdt == MOE_F16)
+    return bwd_tc_t<false>(x_d, offsets, rows, gate, up, down, E, H, I, dy, dinput, dgate, dup,
+                           ddown, scratch, status, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -34,6 +34,14 @@ cudaError_t launch_experts_backward(const void* x_d, const int32_t* offsets, int
                                     int E, int H, int I, const void* dy, void* dinput,
                                     float* dgate, float* dup, float* ddown, float* scratch,
                                     cudaStream_t s);
+// bf16 / f16 expert backward on tensor cores (H % 8 == 0, I % 64 == 0, 16-byte aligned operands);
+// scratch of experts_backward_tc_scratch_bytes(rows, I) bytes, 256-byte aligned.
+size_t experts_backward_tc_scratch_bytes(int64_t rows, int64_t I);
+cudaError_t launch_experts_backward_tc(const void* x_d, const int32_t* offsets, int64_t rows,
+                                       const void* gate, const void* up, const void* down,
+                                       int wdt, int E, int H, int I, const void* dy, void* dinput,
+                                       float* dgate, float* dup, float* ddown, void* scratch,
+                                       unsigned* status, cudaStream_t s);
 cudaError_t launch_combine_backward(const void* y, int ydt, const uint32_t* ros, const void* w,
                                     int wdt, const void* dout, int64_t T, int64_t H, int k,
                                     void* dexpert, float* dweights, cudaStream_t s);

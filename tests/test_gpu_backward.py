@@ -1,8 +1,10 @@
 """GPU parity of the MoE backward chain (ruDNN user guide §12) against the fp64 oracle:
 combine_backward, the expert backward (dinput, FP32 dgate / dup / ddown), dispatch_backward and
-the full chain with the router backward.  Bounds: FP32 outputs (weight gradients, dweights)
-within 1e-4 of the largest |ref|; layer-dtype outputs within the layer tolerance (2e-2 for
-16-bit, 1e-4 for f32) of the largest |ref|."""
+the full chain with the router backward.  Bounds (max |d| / max |ref|): f32 layers 1e-4
+everywhere (FP32 on CUDA cores); 16-bit layers with I % 64 == 0 run on tensor cores, whose
+operands (dy, dg, du, a) are rounded to the layer dtype as the forward rounds a, so every output
+gets the 16-bit layer tolerance 2e-2; other 16-bit shapes (CUDA cores, FP32 operands) keep 1e-4
+for the FP32 weight gradients."""
 import numpy as np
 import pytest
 import torch
@@ -25,7 +27,9 @@ def _groups(counts, seed):
 
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16, torch.float32])
 @pytest.mark.parametrize("counts,H,I", [([70, 0, 129, 5], 96, 160), ([200], 64, 72),
-                                        ([33] * 6, 128, 256), ([0, 0, 3, 0], 40, 24)])
+                                        ([33] * 6, 128, 256), ([0, 0, 3, 0], 40, 24),
+                                        ([300, 0, 129, 77], 256, 384), ([1000], 128, 192),
+                                        ([0, 40, 0, 513, 2], 200, 128)])
 def test_experts_backward_matches_oracle(dt, counts, H, I):
     E = len(counts)
     _, offsets, _, _ = O.dispatch(_groups(counts, sum(counts)), E)
@@ -45,8 +49,9 @@ def test_experts_backward_matches_oracle(dt, counts, H, I):
                                             storage(up)[0], storage(down)[0], name,
                                             O.to_f64(*storage(dy)))
     assert rel_max_err(f64(dx), rdx) <= layer_tol(dt)
+    wtol = layer_tol(dt) if (dt != torch.float32 and I % 64 == 0) else 1e-4
     for got, ref in ((dg, rdg), (du, rdu), (dd, rdd)):
-        assert rel_max_err(f64(got), ref) <= 1e-4
+        assert rel_max_err(f64(got), ref) <= wtol
 
 
 @pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
