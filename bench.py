@@ -202,6 +202,14 @@ def stage_work(wl: W.Workload, n_active: int):
     }
 
 
+def kernel_source_sha256():
+    """SHA-256 over the sources the forward GEMM kernels compile from (kernel + PTX wrappers)."""
+    h = hashlib.sha256()
+    for f in ("experts_tc.cu", "tcgen05.cuh"):
+        h.update(open(os.path.join(ROOT, "mixture_experts_routing_moe_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
 def recorded_traffic():
     """(bytes per launch, kernel hash) from the committed ncu summary, or None."""
     try:
@@ -214,8 +222,7 @@ def recorded_traffic():
             want["bytes"] = float(line.split(":", 1)[1])
         if line.startswith("kernel_source_sha256:"):
             want["sha"] = line.split(":", 1)[1].strip()
-    src = os.path.join(ROOT, "mixture_experts_routing_moe_gb300", "csrc", "experts_tc.cu")
-    cur = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    cur = kernel_source_sha256()
     if "bytes" in want and want.get("sha") == cur:
         return want["bytes"]
     return None
@@ -377,30 +384,50 @@ def run_backward(args):
     for _ in range(max(3, args.warmup)):
         step()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev)
     torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)   # let the sampler take its first reading
     for i in range(args.steps):
         step(evs[i])
     torch.cuda.synchronize()
+    clocks = sampler.stop()
+    st = moe.moe_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
     tot = float(np.mean([e[0].elapsed_time(e[3]) for e in evs]))
     exp_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
     flops = 16 * R * wl.H * wl.I          # recompute g, u (4) + da (2) + dinput (4) + weight grads (6)
-    # FP32 CUDA-core peak from unit counts and clock: SMs x 128 FMA/clk x 2 x max SM clock
-    props = torch.cuda.get_device_properties(dev)
-    peak = props.multi_processor_count * 128 * 2 * 2.07e9 / 1e12
+    tensor = x.dtype != torch.float32 and wl.I % 64 == 0   # the library's tensor-core condition
     achieved = flops / (exp_ms / 1e3) / 1e12
+    if tensor:
+        pk, pk_src = peaks()
+        peak = pk["bf16_tflops_sustained"]
+        roof = {"kernel": "experts backward (tcgen05 GEMMs: dA, gate/up + SwiGLU grad, dinput, "
+                          "weight grads)", "bound": "tensor",
+                "peak_source": f"{pk_src} bf16 sustained (dense, cuBLAS); f16 runs at the bf16 rate"}
+        launches = 9
+    else:
+        # FP32 CUDA-core peak from unit counts and clock: SMs x 128 FMA/clk x 2 x max SM clock
+        props = torch.cuda.get_device_properties(dev)
+        peak = props.multi_processor_count * 128 * 2 * 2.07e9 / 1e12
+        roof = {"kernel": "experts backward (FP32 CUDA-core ragged GEMMs)", "bound": "alu",
+                "peak_source": "derived: SMs x 128 FP32 FMA/clk x 2 x 2.07 GHz"}
+        launches = 10
     line = {"metric": "MoE backward tokens/s (combine, experts, dispatch, router backward)",
             "value": wl.T / (tot / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": tot, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
                        "top_k": wl.top_k},
-            "roofline": {"kernel": "experts backward (FP32 CUDA-core ragged GEMMs)",
-                         "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak,
-                         "peak_source": "derived: SMs x 128 FP32 FMA/clk x 2 x 2.07 GHz",
-                         "traffic": None, "algorithmic_flops_per_launch": flops},
-            "stages_ms": {"experts_backward": exp_ms, "total": tot},
-            "gpu_launches": 10 * args.steps}
+            "roofline": {**roof, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "algorithmic_flops_per_launch": flops},
+            "stages_ms": {"combine_backward": float(np.mean([e[0].elapsed_time(e[1]) for e in evs])),
+                          "experts_backward": exp_ms,
+                          "dispatch_and_router_backward": float(np.mean([e[2].elapsed_time(e[3]) for e in evs])),
+                          "total": tot},
+            "gpu_launches": launches * args.steps, "clocks": clocks}
     print(json.dumps(line), flush=True)
 
 

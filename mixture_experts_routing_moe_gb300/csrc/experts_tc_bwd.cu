@@ -7,12 +7,20 @@
 //   DIN   dinput = [dg du] [gate_e; up_e]       (layer dtype [rows, H]; K = 2I, B read N-major)
 //   WG    dgate_e = dg^T x, dup_e = du^T x, ddown_e = dy^T a   (FP32; both operands M/N-major,
 //         the contraction runs over the expert's rows)
-// One persistent CTA per SM, the warp roles of the forward kernel (TMA producer, MMA issuer,
-// four epilogue warps), 128 x 256 tiles, 4 x 48 KB stages, FP32 accumulators in TMEM.  An
+// Persistent clusters of two CTAs (one per SM), the warp roles of the forward kernel (TMA
+// producer, MMA issuer, four epilogue warps), 128 x 256 tiles, 4 x 48 KB stages, FP32
+// accumulators in TMEM.  The two CTAs of a cluster take two tiles of the same expert that share
+// an operand: two m-tiles of one n-tile (each CTA loads its own A tile and one half of B, which
+// TMA multicasts into both CTAs: 32 KB instead of 48 KB read from L2 per 64-deep K block), or,
+// on an expert's odd last m-tile, two n-tiles of it (A halves multicast, own B).  A stage is
+// refilled once the MMAs of both CTAs have consumed it (the commits are multicast).  An
 // operand whose contiguous dimension is M or N is loaded as 64-column boxes and described as an
 // MN-major 128-byte-swizzled matrix (boxes 8 KB apart, 8-row groups 1 KB apart).  In WG the last
 // 64-row K block of an expert would run into the next expert's rows: the MMA warp zeroes those
-// rows in shared memory before the MMAs read them.  All waits are bounded as in the forward.
+// rows in shared memory before the MMAs read them.  WG epilogue warps stage each 32 x 32 FP32
+// chunk in shared memory (128-byte swizzle) and write it with a TMA tensor store through a
+// [E][M][N] map, so every store moves whole 128-byte lines and never crosses into the next
+// expert's slice.  All waits are bounded as in the forward.
 #include <type_traits>
 
 #include "common.cuh"
@@ -30,10 +38,18 @@ constexpr int BOX_BYTES = 64 * 128;  // one 64-row x 64-column box
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
-constexpr size_t kSmemBytes =
-    1024 + (size_t)STAGES * STAGE_BYTES + 256 + (kMaxExperts + 4) * sizeof(int);
+constexpr int kChunkBytes = 32 * 32 * 4;             // one 32-row x 32-column FP32 store box
+constexpr int kStagingBytes = 4 * 2 * kChunkBytes;   // two store buffers per epilogue warp
 
 enum Mode { DA = 0, GU = 1, DIN = 2, WG = 3 };
+
+// WG: stages | store buffers | barriers.  Others: stages | barriers | m-tile prefix.
+template <int MODE>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)STAGES * STAGE_BYTES + (MODE == WG ? kStagingBytes : 0) + 256 +
+         (MODE == WG ? 0 : (kMaxExperts + 4) * sizeof(int));
+}
+static_assert(smem_bytes<WG>() <= 232448 && smem_bytes<DA>() <= 232448, "shared memory");
 
 // MN-major 128-byte-swizzled operand: 64-column boxes BOX_BYTES apart, 8-row groups 1 KB apart.
 __device__ __forceinline__ uint64_t make_sdesc_mn(uint32_t saddr) {
@@ -49,7 +65,8 @@ struct BwdParams {
   const int32_t* offsets;
   int E, H, I;
   int KB;           // K blocks (DA: H/64, GU: H/64, DIN: 2I/64); WG: per expert
-  int NT, MT;       // n-tiles per expert (and m-tiles per expert in WG)
+  int NT;           // n-tiles per expert
+  int MP;           // WG: m-tile pairs per expert
   int M, N;         // WG: output matrix of each expert is M x N
   int a_col0;       // WG: first column of A inside its source matrix (du starts at I)
   const float* da;  // GU: da [rows, I] FP32
@@ -58,35 +75,67 @@ struct BwdParams {
   unsigned* status;
 };
 
+// Pair tile t -> expert e (rows r0 .. r1-1), this CTA's m-tile and n-tile, and which operand the
+// pair shares.  WG: m-tiles 2 mp + rank of the expert's output share B.  Other modes: an expert
+// with mt m-tiles has floor(mt / 2) * NT "m-pairs" (m-tiles 2 mp + rank, one n-tile, B shared)
+// and, when mt is odd, ceil(NT / 2) "n-pairs" on its last m-tile (n-tiles 2 q + rank, A shared),
+// so no pair computes a whole m-tile of rows that are not the expert's.  A tile past the
+// expert's last m-tile or n-tile is computed on rows or columns of no interest and not stored.
 template <int MODE>
-__device__ __forceinline__ void decode(int t, const int* pref, const BwdParams& p, int& e, int& m,
-                                       int& n) {
+__device__ __forceinline__ void decode(int t, const int* pref, const BwdParams& p, uint32_t rank,
+                                       int& e, int& r0, int& r1, int& m, int& n, bool& share_a) {
+  share_a = false;
   if (MODE == WG) {
-    const int per = p.MT * p.NT;
+    const int per = p.MP * p.NT;
     e = t / per;
     const int r = t - e * per;
-    m = r / p.NT;
-    n = r - m * p.NT;
-  } else {  // expert rows in 128-row tiles, n inner: CTAs in flight share an A tile
-    const int j = t / p.NT;
-    e = find_expert(pref, p.E, j);
-    m = j - pref[e];
-    n = t - j * p.NT;
+    const int mp = r / p.NT;
+    n = r - mp * p.NT;
+    m = 2 * mp + (int)rank;
+    r0 = __ldg(p.offsets + e);
+    r1 = __ldg(p.offsets + e + 1);
+  } else {
+    e = find_expert(pref, p.E, t);
+    r0 = __ldg(p.offsets + e);
+    r1 = __ldg(p.offsets + e + 1);
+    const int local = t - pref[e];
+    const int mt = (r1 - r0 + BM - 1) / BM, full = (mt >> 1) * p.NT;
+    if (local < full) {  // n inner: clusters in flight share the A tiles
+      const int mp = local / p.NT;
+      n = local - mp * p.NT;
+      m = 2 * mp + (int)rank;
+    } else {
+      m = mt - 1;
+      n = 2 * (local - full) + (int)rank;
+      share_a = true;
+    }
   }
 }
+
+// Pair tiles of an expert with n rows (modes other than WG).
+struct PairTiles {
+  int NT;
+  __device__ int operator()(int n) const {
+    const int mt = (n + BM - 1) / BM;
+    return (mt >> 1) * NT + (mt & 1) * ((NT + 1) >> 1);
+  }
+};
 
 template <int MODE, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_experts_bwd_tc(const __grid_constant__ CUtensorMap mapA,
                        const __grid_constant__ CUtensorMap mapB0,
-                       const __grid_constant__ CUtensorMap mapB1, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap mapB1,
+                       const __grid_constant__ CUtensorMap mapX, const BwdParams p) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
   constexpr bool A_MN = MODE == WG, B_MN = MODE != GU;
   extern __shared__ uint8_t tcb_smem_raw[];
   const uint32_t raw = smem_u32(tcb_smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = tcb_smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * STAGE_BYTES);
+  const uint32_t staging = base + STAGES * STAGE_BYTES;  // WG store buffers (1 KB aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * STAGE_BYTES +
+                                               (MODE == WG ? kStagingBytes : 0));
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
@@ -98,10 +147,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* pref = reinterpret_cast<int*>(tmem_slot + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int pair = (int)cluster_id_x(), npairs = (int)ncluster_x();
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), 2);  // the MMA commits of both CTAs
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -112,17 +163,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-  if (warp == 2 && MODE != WG) build_mtile_prefix(p.offsets, p.E, BM, pref, lane);
+  if (warp == 2 && MODE != WG) build_expert_prefix(p.offsets, p.E, PairTiles{p.NT}, pref, lane);
   if (warp == 0 && lane == 0) {
     tma_prefetch(&mapA);
     tma_prefetch(&mapB0);
     tma_prefetch(&mapB1);
+    tma_prefetch(&mapX);
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();  // both CTAs: barriers initialised before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = MODE == WG ? p.E * p.MT * p.NT : pref[p.E] * p.NT;
+  const int total = MODE == WG ? p.E * p.MP * p.NT : pref[p.E];
 
   if (warp == 0) {
     if (lane == 0) {
@@ -131,10 +183,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool stop = false;
       const uint64_t pol = policy_evict_normal();
-      for (int t = blockIdx.x; t < total && !stop; t += gridDim.x) {
-        int e, m, n;
-        decode<MODE>(t, pref, p, e, m, n);
-        const int r0 = __ldg(p.offsets + e), r1 = __ldg(p.offsets + e + 1);
+      for (int t = pair; t < total && !stop; t += npairs) {
+        int e, r0, r1, m, n;
+        bool share_a;
+        decode<MODE>(t, pref, p, rank, e, r0, r1, m, n, share_a);
         const int KB = MODE == WG ? (r1 - r0 + BK - 1) / BK : p.KB;
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_f, p.status)) {
@@ -147,14 +199,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int y = r0 + kb * BK;
             for (int j = 0; j < 2; ++j)
               tma_load_2d(sa + j * BOX_BYTES, &mapA, full_bar(stage), p.a_col0 + m * BM + 64 * j, y, pol);
-            for (int j = 0; j < 4; ++j)
-              tma_load_2d(sb + j * BOX_BYTES, &mapB0, full_bar(stage), n * BN + 64 * j, y, pol);
+            for (int j = 2 * (int)rank; j < 2 * (int)rank + 2; ++j)  // this CTA's half of B
+              tma_load_2d_mc(sb + j * BOX_BYTES, &mapB0, full_bar(stage), n * BN + 64 * j, y,
+                             0x3, pol);
           } else {
-            tma_load_2d(sa, &mapA, full_bar(stage), kb * BK, r0 + m * BM, pol);
+            // m-pair: own A tile, half of the shared B.  n-pair: half of the shared A (64 rows,
+            // through the 64-row map), own B.
+            if (share_a)
+              tma_load_2d_mc(sa + rank * (A_BYTES / 2), &mapX, full_bar(stage), kb * BK,
+                             r0 + m * BM + 64 * (int)rank, 0x3, pol);
+            else
+              tma_load_2d(sa, &mapA, full_bar(stage), kb * BK, r0 + m * BM, pol);
+            const int jb0 = share_a ? 0 : 2 * (int)rank, jb1 = share_a ? 4 : jb0 + 2;
             if (MODE == GU) {  // K-major: 128 gate rows then the same 128 up rows
               const int br = e * p.I + n * (BN / 2);
-              tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, br, pol);
-              tma_load_2d(sb + B_BYTES / 2, &mapB1, full_bar(stage), kb * BK, br, pol);
+              if (share_a) {
+                tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, br, pol);
+                tma_load_2d(sb + B_BYTES / 2, &mapB1, full_bar(stage), kb * BK, br, pol);
+              } else {  // rank 0 loads the gate half, rank 1 the up half
+                tma_load_2d_mc(sb + rank * (B_BYTES / 2), rank == 0 ? &mapB0 : &mapB1,
+                               full_bar(stage), kb * BK, br, 0x3, pol);
+              }
             } else {
               // N-major B: rows are K.  DA: down [E*H, I];  DIN: gate (k < I) / up (k >= I)
               const CUtensorMap* mb = &mapB0;
@@ -166,8 +231,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (k0 >= p.I) mb = &mapB1;
                 kr = e * p.I + (k0 >= p.I ? k0 - p.I : k0);
               }
-              for (int j = 0; j < 4; ++j)
-                tma_load_2d(sb + j * BOX_BYTES, mb, full_bar(stage), n * BN + 64 * j, kr, pol);
+              for (int j = jb0; j < jb1; ++j) {  // all of B (n-pair) or this CTA's half
+                if (share_a)
+                  tma_load_2d(sb + j * BOX_BYTES, mb, full_bar(stage), n * BN + 64 * j, kr, pol);
+                else
+                  tma_load_2d_mc(sb + j * BOX_BYTES, mb, full_bar(stage), n * BN + 64 * j, kr,
+                                 0x3, pol);
+              }
             }
           }
           ++armed;
@@ -195,10 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool stop = false;
-    for (int t = blockIdx.x; t < total && !stop; t += gridDim.x) {
-      int e, m, n;
-      decode<MODE>(t, pref, p, e, m, n);
-      const int r0 = __ldg(p.offsets + e), r1 = __ldg(p.offsets + e + 1);
+    for (int t = pair; t < total && !stop; t += npairs) {
+      int e, r0, r1, m, n;
+      bool share_a;
+      decode<MODE>(t, pref, p, rank, e, r0, r1, m, n, share_a);
       const int KB = MODE == WG ? (r1 - r0 + BK - 1) / BK : p.KB;
       bool ok = lane != 0 || wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_f, p.status);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
@@ -234,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BK / 16; ++kk)  // 16 K: 32 bytes (K-major) or 2 KB (MN-major)
             umma_f16(d_tmem, da + (A_MN ? 128u : 2u) * kk, db + (B_MN ? 128u : 2u) * kk, idesc,
                      (kb | kk) != 0);
-          umma_commit(empty_bar(stage));
+          umma_commit_mc(empty_bar(stage), 0x3);  // frees the stage in both CTAs
         }
         __syncwarp();
         if (++stage == STAGES) {
@@ -255,33 +325,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------------- epilogue (warps 2..5)
     const int q = warp & 3;
-    int acc = 0;
+    int acc = 0, slot = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      int e, m, n;
-      decode<MODE>(t, pref, p, e, m, n);
+    for (int t = pair; t < total; t += npairs) {
+      int e, r0, r1, m, n;
+      bool share_a;
+      decode<MODE>(t, pref, p, rank, e, r0, r1, m, n, share_a);
       const bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_f, p.status);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
-      const int r0 = __ldg(p.offsets + e), r1 = __ldg(p.offsets + e + 1);
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
       if (MODE == WG) {
-        const int mrow = m * BM + q * 32 + lane;  // output row of C_e
-        const bool empty = r1 == r0;              // no rows: the gradient is zero
-        float* crow = reinterpret_cast<float*>(p.out0) + ((size_t)e * p.M + mrow) * p.N;
+        // rows m*BM + q*32 .. +31 of C_e; chunk c covers columns n*BN + 32c .. +31
+        const int row0 = m * BM + q * 32;
+        const bool empty = r1 == r0;  // no rows: the gradient is zero
+        if (row0 < p.M) {
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c * 32, r);
-          tmem_wait_ld();
-          const int col0 = n * BN + c * 32;
-          if (mrow < p.M) {
+          for (int c = 0; c < 8; ++c) {
+            const int col0 = n * BN + c * 32;
+            if (col0 >= p.N) break;
+            uint32_t r[32];
+            tmem_ld32(taddr + c * 32, r);
+            tmem_wait_ld();
+            const uint32_t buf = staging + (uint32_t)((q * 2 + slot) * kChunkBytes);
+            if (lane == 0) bulk_wait_read<1>();  // the store that last read `buf` is done with it
+            __syncwarp();
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              if (col0 + v * 4 < p.N)
-                st_v4(crow + col0 + v * 4,
-                      empty ? make_uint4(0, 0, 0, 0)
-                            : make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]));
+            for (int j = 0; j < 8; ++j) {  // 16-byte chunk j of this lane's row, 128-byte swizzle
+              const uint32_t dst = buf + lane * 128 + ((j ^ (lane & 7)) << 4);
+              if (empty)
+                st_shared_v4(dst, 0u, 0u, 0u, 0u);
+              else
+                st_shared_v4(dst, r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&mapX, buf, col0, row0, e);
+              bulk_commit();
+            }
+            slot ^= 1;
           }
         }
       } else {
@@ -369,27 +452,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (MODE == WG && lane == 0) bulk_wait_all();  // stores done before shared memory goes away
   }
 
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cluster_sync_all();  // no CTA leaves while its pair may still write to it or signal it
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
+// Launches clusters of two CTAs, at most as many as can be resident at once (queried once per
+// device and mode); `upper_pairs` bounds the number of pair tiles.  `x` is the TMA store map of
+// the weight gradient (WG) or the 64-row-box map of A that n-pair tiles load halves through.
 template <int MODE, bool BF16>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                        const BwdParams& p, int64_t upper_tiles, int sms, cudaStream_t s) {
+                        const CUtensorMap& c, const BwdParams& p, int64_t upper_pairs, int dev,
+                        cudaStream_t s) {
   auto kern = moe_experts_bwd_tc<MODE, BF16>;
+  constexpr size_t smem = smem_bytes<MODE>();
   cudaError_t err =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  const int grid = (int)(upper_tiles < sms ? upper_tiles : sms);
-  if (grid < 1) return cudaSuccess;
-  kern<<<grid, kThreads, kSmemBytes, s>>>(a, b0, b1, p);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2);
+  static int max_pairs[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_pairs[dev] == 0) {
+    int n = 0;
+    err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (err != cudaSuccess) return err;
+    if (n < 1) return cudaErrorLaunchOutOfResources;
+    max_pairs[dev] = n;
+  }
+  const int pairs = (int)(upper_pairs < max_pairs[dev] ? upper_pairs : max_pairs[dev]);
+  if (pairs < 1) return cudaSuccess;
+  cfg.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, c, p);
 }
 
 template <bool BF16>
@@ -397,16 +508,15 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
                      const void* up, const void* down, int E, int H, int I, const void* dy,
                      void* dinput, float* dgate, float* dup, float* ddown, void* scratch,
                      unsigned* status, cudaStream_t s) {
-  int dev = 0, sms = 0;
+  int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
   // scratch: da FP32 [rows, I] | dgdu [rows, 2I] | a [rows, I] (layer dtype)
   float* da = (float*)scratch;
   uint8_t* dgdu = (uint8_t*)scratch + align_up((size_t)rows * I * 4, 256);
   uint8_t* abuf = dgdu + align_up((size_t)rows * 2 * I * 2, 256);
-  const int64_t mt_upper = (rows + BM - 1) / BM + E;
+  const int64_t mt_upper = (rows + BM - 1) / BM + E;  // >= m-tiles; pair tiles <= mt * ceil(NT/2)
+  CUtensorMap mAh;  // A with 64-row boxes: the halves of a shared A tile
   CUtensorMap mA, mB0, mB1;
   BwdParams p{};
   p.offsets = offsets;
@@ -417,16 +527,18 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
 
   // 1. da = dy down_e
   if (!make_map_2d(&mA, dy, BF16, H, rows, BK, BM) ||
+      !make_map_2d(&mAh, dy, BF16, H, rows, BK, BM / 2) ||
       !make_map_2d(&mB0, down, BF16, I, (int64_t)E * H, 64, 64))
     return cudaErrorInvalidValue;
   p.KB = (H + BK - 1) / BK;
   p.NT = (I + BN - 1) / BN;
   p.out0 = da;
-  err = launch_mode<DA, BF16>(mA, mB0, mB0, p, mt_upper * p.NT, sms, s);
+  err = launch_mode<DA, BF16>(mA, mB0, mB0, mAh, p, mt_upper * ((p.NT + 1) / 2), dev, s);
   if (err != cudaSuccess) return err;
 
   // 2. g, u recomputed; epilogue -> dg | du, a
   if (!make_map_2d(&mA, x_d, BF16, H, rows, BK, BM) ||
+      !make_map_2d(&mAh, x_d, BF16, H, rows, BK, BM / 2) ||
       !make_map_2d(&mB0, gate, BF16, H, (int64_t)E * I, BK, BN / 2) ||
       !make_map_2d(&mB1, up, BF16, H, (int64_t)E * I, BK, BN / 2))
     return cudaErrorInvalidValue;
@@ -435,48 +547,52 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
   p.da = da;
   p.out0 = dgdu;
   p.out1 = abuf;
-  err = launch_mode<GU, BF16>(mA, mB0, mB1, p, mt_upper * p.NT, sms, s);
+  err = launch_mode<GU, BF16>(mA, mB0, mB1, mAh, p, mt_upper * ((p.NT + 1) / 2), dev, s);
   if (err != cudaSuccess) return err;
 
   // 3. dinput = [dg du] [gate_e; up_e]
   if (!make_map_2d(&mA, dgdu, BF16, 2 * (int64_t)I, rows, BK, BM) ||
+      !make_map_2d(&mAh, dgdu, BF16, 2 * (int64_t)I, rows, BK, BM / 2) ||
       !make_map_2d(&mB0, gate, BF16, H, (int64_t)E * I, 64, 64) ||
       !make_map_2d(&mB1, up, BF16, H, (int64_t)E * I, 64, 64))
     return cudaErrorInvalidValue;
   p.KB = 2 * I / BK;
   p.NT = (H + BN - 1) / BN;
   p.out0 = dinput;
-  err = launch_mode<DIN, BF16>(mA, mB0, mB1, p, mt_upper * p.NT, sms, s);
+  err = launch_mode<DIN, BF16>(mA, mB0, mB1, mAh, p, mt_upper * ((p.NT + 1) / 2), dev, s);
   if (err != cudaSuccess) return err;
 
   // 4. weight gradients, contracted over each expert's rows
-  CUtensorMap mX;
+  CUtensorMap mX, mC;
   if (!make_map_2d(&mA, dgdu, BF16, 2 * (int64_t)I, rows, 64, 64) ||
-      !make_map_2d(&mX, x_d, BF16, H, rows, 64, 64))
+      !make_map_2d(&mX, x_d, BF16, H, rows, 64, 64) ||
+      !make_map_3d_f32(&mC, dgate, H, I, E, 32, 32))
     return cudaErrorInvalidValue;
   p.M = I;
   p.N = H;
-  p.MT = (I + BM - 1) / BM;
+  p.MP = (I + 2 * BM - 1) / (2 * BM);
   p.NT = (H + BN - 1) / BN;
   p.out0 = dgate;
   p.a_col0 = 0;
-  err = launch_mode<WG, BF16>(mA, mX, mX, p, (int64_t)E * p.MT * p.NT, sms, s);
+  err = launch_mode<WG, BF16>(mA, mX, mX, mC, p, (int64_t)E * p.MP * p.NT, dev, s);
   if (err != cudaSuccess) return err;
+  if (!make_map_3d_f32(&mC, dup, H, I, E, 32, 32)) return cudaErrorInvalidValue;
   p.out0 = dup;
   p.a_col0 = I;
-  err = launch_mode<WG, BF16>(mA, mX, mX, p, (int64_t)E * p.MT * p.NT, sms, s);
+  err = launch_mode<WG, BF16>(mA, mX, mX, mC, p, (int64_t)E * p.MP * p.NT, dev, s);
   if (err != cudaSuccess) return err;
   CUtensorMap mY, mAct;
   if (!make_map_2d(&mY, dy, BF16, H, rows, 64, 64) ||
-      !make_map_2d(&mAct, abuf, BF16, I, rows, 64, 64))
+      !make_map_2d(&mAct, abuf, BF16, I, rows, 64, 64) ||
+      !make_map_3d_f32(&mC, ddown, I, H, E, 32, 32))
     return cudaErrorInvalidValue;
   p.M = H;
   p.N = I;
-  p.MT = (H + BM - 1) / BM;
+  p.MP = (H + 2 * BM - 1) / (2 * BM);
   p.NT = (I + BN - 1) / BN;
   p.out0 = ddown;
   p.a_col0 = 0;
-  return launch_mode<WG, BF16>(mY, mAct, mAct, p, (int64_t)E * p.MT * p.NT, sms, s);
+  return launch_mode<WG, BF16>(mY, mAct, mAct, mC, p, (int64_t)E * p.MP * p.NT, dev, s);
 }
 
 }  // namespace
