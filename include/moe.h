@@ -210,12 +210,26 @@ int moe_combine(const void* y, int ydt, const uint32_t* row_of_slot, const void*
  * x [T, H] and the expert weights share dtype `wdt`; logits [T, E] have dtype `ldt`;
  * out [T, H] has dtype `wdt`.  Same alignment rules as the stages.
  * ws: at least moe_forward_workspace_bytes(T, E, H, I, top_k, ldt, wdt) bytes, 256-byte aligned.
+ * Short batches (see moe_forward_fused) run as ONE cooperative launch that performs the same
+ * steps between grid barriers; longer ones as the staged launches.  Both give the same routing,
+ * dispatch order and combine order.
  */
 size_t moe_forward_workspace_bytes(int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
                                    int ldt, int wdt);
 int moe_forward(const void* x, const void* logits, int ldt, const void* gate, const void* up,
                 const void* down, int wdt, int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
                 int renormalize, void* out, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_forward_fused — 1 when moe_forward runs these sizes as the single fused launch, else 0
+ * (given 16-byte aligned logits, x, weights and out).  That is: bf16/f16 experts, T*top_k <= 4096
+ * and fewer than 128 rows per expert on average (T*top_k < 128 E), E <= 256 with E * sizeof(ldt)
+ * a multiple of 16, H and I multiples of 64, and a device with cooperative launch.  Otherwise 0.
+ * The fused route reads each row of logits with one full warp; for 64 < E <= 256 and 16-bit
+ * logits that is the staged route's arithmetic exactly, elsewhere the softmax denominator of a
+ * non-renormalised route may be summed in another order (last-ulp differences in w).
+ */
+int moe_forward_fused(int64_t T, int64_t E, int64_t H, int64_t I, int top_k, int ldt, int wdt);
 
 /*
  * moe_forward_sigmoid_grouped — SwiGluExperts::forward_sigmoid_grouped of §10: group-limited
@@ -249,7 +263,10 @@ int moe_combine_backward(const void* y, int ydt, const uint32_t* row_of_slot, co
  *   da = dy down_e;  s = sigmoid(g);  du = da * g s;  dg = da * u * s (1 + g (1 - s))
  *   dinput = dg gate_e + du up_e                 ([rows, H], dtype wdt)
  *   ddown[e] = dy^T (g s u); dgate[e] = dg^T x_d; dup[e] = du^T x_d   (FP32, [E,H,I], [E,I,H] x2)
- * computed with FP32 accumulation on CUDA cores.  Experts without rows get zero gradients.
+ * with FP32 accumulation: on tensor cores (tcgen05) for bf16/f16 with I % 64 == 0 and 16-byte
+ * aligned operands, whose GEMM operands dy, dg, du and g s u are then rounded to `wdt` as the
+ * forward rounds a; on CUDA cores with FP32 operands otherwise.  Experts without rows get zero
+ * gradients.
  * dy [rows, H] dtype wdt.  ws: moe_experts_backward_workspace_bytes(rows, I), 256-byte aligned.
  */
 size_t moe_experts_backward_workspace_bytes(int64_t rows, int64_t I);
@@ -267,11 +284,12 @@ int moe_dispatch_backward(const void* dinput, int dt, const uint32_t* row_of_slo
                           int64_t H, int top_k, void* dx, moe_stream_t stream);
 
 /*
- * moe_forward_with_events — moe_forward that also records caller-created CUDA events
- * (cudaEvent_t, passed as void*) on `stream` at the stage boundaries, for timing:
+ * moe_forward_with_events — the staged path of moe_forward (route, dispatch, gate/up GEMM, down
+ * GEMM and combine as separate launches, whatever the sizes) that also records caller-created
+ * CUDA events (cudaEvent_t, passed as void*) on `stream` at the stage boundaries, for timing:
  *   events[0] before the route      events[1] after the route     events[2] after dispatch
  *   events[3] after the gate/up GEMM events[4] after the down GEMM events[5] after the combine
- * `events` may be NULL (then this is moe_forward).  The launched work is identical.
+ * `events` may be NULL (then this runs the staged path untimed).
  */
 int moe_forward_with_events(const void* x, const void* logits, int ldt, const void* gate,
                             const void* up, const void* down, int wdt, int64_t T, int64_t E,

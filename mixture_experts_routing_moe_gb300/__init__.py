@@ -6,6 +6,7 @@ The compute lives in ``libmoe.so`` (hand-written CUDA kernels behind the C ABI d
 from .binding import (MoeError, moe_combine_backward, moe_dispatch_backward,  # noqa: F401
                       moe_experts_backward, dispatch_workspace_bytes, experts_workspace_bytes,  # noqa: F401
                       forward_workspace_bytes, moe_combine, moe_device_status, moe_dispatch,
-                      moe_experts_forward_dispatched, moe_forward, moe_forward_sigmoid_grouped,
+                      moe_experts_forward_dispatched, moe_forward, moe_forward_fused,
+                      moe_forward_sigmoid_grouped,
                       moe_forward_with_events, moe_route, moe_route_sigmoid_grouped,
                       moe_selected_router_backward, moe_selected_router_weights)

@@ -52,6 +52,7 @@ _SIGS = {
                                            _vp, _sz, _vp]),
     "moe_forward_with_events": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _int, _i64, _i64, _i64,
                                        _i64, _int, _int, _vp, _vp, _sz, _vp, _vp]),
+    "moe_forward_fused": (_int, [_i64, _i64, _i64, _i64, _int, _int, _int]),
     "moe_combine_backward": (_int, [_vp, _int, _vp, _vp, _int, _vp, _i64, _i64, _int, _vp, _vp,
                                     _vp]),
     "moe_experts_backward_workspace_bytes": (_sz, [_i64, _i64]),
@@ -295,19 +296,32 @@ def moe_forward_sigmoid_grouped(x, logits, gate, up, down, top_k: int, groups: i
     return out
 
 
-def moe_forward_with_events(x, logits, gate, up, down, top_k: int, renormalize: bool, out, ws,
-                            events, stream=None):
-    """moe_forward recording six torch.cuda.Event objects at the stage boundaries
-    (before route / after route / after dispatch / after gate-up / after down / after combine)."""
-    _cuda(x, logits, gate, up, down, out, ws)
+def moe_forward_fused(T: int, E: int, H: int, I: int, top_k: int, logits_dtype, dtype) -> bool:
+    """Whether moe_forward runs these sizes as the single fused launch (aligned tensors)."""
+    return bool(lib().moe_forward_fused(T, E, H, I, top_k, DTYPE_CODE[logits_dtype], DTYPE_CODE[dtype]))
+
+
+def moe_forward_with_events(x, logits, gate, up, down, top_k: int, renormalize: bool, out=None,
+                            ws=None, events=None, stream=None):
+    """The staged moe_forward (separate launches), recording six torch.cuda.Event objects at the
+    stage boundaries (before route / after route / after dispatch / after gate-up / after down /
+    after combine) when `events` is given."""
+    _cuda(x, logits, gate, up, down)
     T, H = x.shape
     E, I, _ = gate.shape
-    if len(events) != 6:
-        raise ValueError("moe_forward_with_events needs six events")
-    for ev in events:
-        if ev.cuda_event == 0:      # torch creates the CUDA event on its first record
-            ev.record(torch.cuda.current_stream() if stream is None else stream)
-    arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
+    out = torch.empty_like(x) if out is None else out
+    if ws is None:
+        ws = torch.empty(max(forward_workspace_bytes(T, E, H, I, top_k, logits.dtype, x.dtype), 256),
+                         dtype=torch.uint8, device=x.device)
+    _cuda(out, ws)
+    arr = None
+    if events is not None:
+        if len(events) != 6:
+            raise ValueError("moe_forward_with_events needs six events")
+        for ev in events:
+            if ev.cuda_event == 0:      # torch creates the CUDA event on its first record
+                ev.record(torch.cuda.current_stream() if stream is None else stream)
+        arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
     _check(lib().moe_forward_with_events(
         _ptr(x), _ptr(logits), _code(logits), _ptr(gate), _ptr(up), _ptr(down), _code(gate), T, E,
         H, I, top_k, int(bool(renormalize)), _ptr(out), _ptr(ws), ws.numel(), _stream(stream),

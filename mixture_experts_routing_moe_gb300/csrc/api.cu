@@ -104,10 +104,29 @@ bool record(void* const* events, int i, cudaStream_t s) {
 }
 
 // The fused forward: route (softmax or sigmoid), dispatch, experts, combine on one stream.
+// Whether moe_forward runs the single-launch fused path (softmax routing, no stage events).
+bool takes_fused(const RouteSpec& rs, int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
+                 int ldt, int wdt) {
+  if (rs.sigmoid || !valid_dtype(ldt) || !valid_dtype(wdt)) return false;
+  if (E > kFusedDecodeMaxExperts || H > INT32_MAX || I > INT32_MAX) return false;
+  if (!fused_decode_supported(T, (int)E, H, I, top_k, ldt, wdt)) return false;
+  static int coop[64] = {};  // 1: cooperative launch supported, 2: not (per device)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (coop[dev] == 0) {
+    int v = 0;
+    coop[dev] = (cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess &&
+                 v)
+                    ? 1
+                    : 2;
+  }
+  return coop[dev] == 1;
+}
+
 int run_forward(const void* x, const void* logits, int ldt, const void* gate, const void* up,
                 const void* down, int wdt, int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
                 const RouteSpec& rs, void* out, void* ws, size_t ws_bytes, cudaStream_t s,
-                void* const* events) {
+                void* const* events, bool allow_fused) {
   if (!valid_dtype(ldt) || !valid_dtype(wdt)) return MOE_ERR_DTYPE;
   int st = check_experts_shape(T * top_k, E, H, I);
   if (st != MOE_OK) return st;
@@ -135,6 +154,33 @@ int run_forward(const void* x, const void* logits, int ldt, const void* gate, co
   void* a = b + L.a;
   const int64_t R = T * top_k;
 
+  if (allow_fused && !events && aligned16(logits) &&
+      takes_fused(rs, T, E, H, I, top_k, ldt, wdt)) {
+    // status word at byte 0 and the grid-barrier counter at byte 64 of the header, both zeroed
+    if (cudaMemsetAsync(ws, 0, 128, s) != cudaSuccess) return MOE_ERR_CUDA;
+    FusedDecodeArgs f{};
+    f.logits = logits;
+    f.x = x;
+    f.gate = gate;
+    f.up = up;
+    f.down = down;
+    f.T = T;
+    f.E = (int)E;
+    f.H = (int)H;
+    f.I = (int)I;
+    f.k = top_k;
+    f.renorm = rs.renormalize != 0;
+    f.idx = idx;
+    f.w = w;
+    f.row_of_slot = ros;
+    f.offsets = offsets;
+    f.x_d = xd;
+    f.a = a;
+    f.out = out;
+    f.status = status;
+    f.grid_count = (unsigned*)(b + 64);
+    return cuda_status(launch_decode_fused(f, ldt, wdt, s));
+  }
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return MOE_ERR_CUDA;
   if (!record(events, 0, s)) return MOE_ERR_CUDA;
   cudaError_t err =
@@ -337,8 +383,18 @@ size_t moe_forward_workspace_bytes(int64_t T, int64_t E, int64_t H, int64_t I, i
 int moe_forward(const void* x, const void* logits, int ldt, const void* gate, const void* up,
                 const void* down, int wdt, int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
                 int renormalize, void* out, void* ws, size_t ws_bytes, moe_stream_t stream) {
-  return moe_forward_with_events(x, logits, ldt, gate, up, down, wdt, T, E, H, I, top_k,
-                                 renormalize, out, ws, ws_bytes, stream, nullptr);
+  const int st = check_route_shape(T, E, top_k);
+  if (st != MOE_OK) return st;
+  const RouteSpec r{false, renormalize, nullptr, 1, 1, 0, 1.f};
+  return run_forward(x, logits, ldt, gate, up, down, wdt, T, E, H, I, top_k, r, out, ws, ws_bytes,
+                     (cudaStream_t)stream, nullptr, /*allow_fused=*/true);
+}
+
+int moe_forward_fused(int64_t T, int64_t E, int64_t H, int64_t I, int top_k, int ldt, int wdt) {
+  if (check_route_shape(T, E, top_k) != MOE_OK || check_experts_shape(T * top_k, E, H, I) != MOE_OK)
+    return 0;
+  const RouteSpec r{false, 1, nullptr, 1, 1, 0, 1.f};
+  return takes_fused(r, T, E, H, I, top_k, ldt, wdt) ? 1 : 0;
 }
 
 int moe_forward_with_events(const void* x, const void* logits, int ldt, const void* gate,
@@ -349,7 +405,7 @@ int moe_forward_with_events(const void* x, const void* logits, int ldt, const vo
   if (st != MOE_OK) return st;
   const RouteSpec r{false, renormalize, nullptr, 1, 1, 0, 1.f};
   return run_forward(x, logits, ldt, gate, up, down, wdt, T, E, H, I, top_k, r, out, ws, ws_bytes,
-                     (cudaStream_t)stream, events);
+                     (cudaStream_t)stream, events, /*allow_fused=*/false);
 }
 
 int moe_forward_sigmoid_grouped(const void* x, const void* logits, int ldt, const float* bias,
@@ -363,7 +419,7 @@ int moe_forward_sigmoid_grouped(const void* x, const void* logits, int ldt, cons
   if (st != MOE_OK) return st;
   const RouteSpec r{true, renormalize, bias, groups, selected_groups, group_top_two, scale};
   return run_forward(x, logits, ldt, gate, up, down, wdt, T, E, H, I, top_k, r, out, ws, ws_bytes,
-                     (cudaStream_t)stream, nullptr);
+                     (cudaStream_t)stream, nullptr, /*allow_fused=*/false);
 }
 
 int moe_combine_backward(const void* y, int ydt, const uint32_t* row_of_slot, const void* w,

@@ -5,6 +5,7 @@
 // output dtype.  A token is spread over ceil(H / (32 * 16-byte chunk)) warps, one 16-byte column
 // chunk per lane, so short batches still fill the GPU; each warp loads the token's k
 // (row, weight) pairs through its lanes and broadcasts them with shuffles.
+#include "combine_core.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -22,55 +23,8 @@ __global__ void __launch_bounds__(kCombWarps * 32)
   const int64_t gw = (int64_t)blockIdx.x * kCombWarps + (threadIdx.x >> 5);
   const int64_t t = gw / warps_per_token;
   if (t >= T) return;
-  constexpr int VW = VEC ? 16 / (int)sizeof(TY) : 1;
-  const int64_t chunks = H / VW;
-  const int64_t c = (gw - t * warps_per_token) * 32 + lane;  // this lane's column chunk
-  float acc[VW];
-#pragma unroll
-  for (int i = 0; i < VW; ++i) acc[i] = 0.f;
-  bool poisoned = false;
-  for (int jb = 0; jb < k; jb += 32) {
-    uint32_t my_row = kInvalidRow;
-    float my_w = 0.f;
-    if (jb + lane < k) {
-      my_row = row_of_slot[t * k + jb + lane];
-      my_w = Dt<TW>::to_f(w[t * k + jb + lane]);
-    }
-    const int nj = min(32, k - jb);
-    for (int jj = 0; jj < nj; ++jj) {
-      const uint32_t r = __shfl_sync(0xFFFFFFFFu, my_row, jj);
-      const float wj = __shfl_sync(0xFFFFFFFFu, my_w, jj);
-      if (r == kInvalidRow) {
-        poisoned = true;
-        continue;
-      }
-      if (c < chunks) {
-        if (VEC) {
-          Vec16<TY> q;
-          q.u = ld_nc_v4(y + (int64_t)r * H + c * VW);
-          float f[VW];
-          q.to_float(f);
-#pragma unroll
-          for (int i = 0; i < VW; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
-        } else {
-          acc[0] = fmaf(wj, Dt<TY>::to_f(y[(int64_t)r * H + c]), acc[0]);
-        }
-      }
-    }
-  }
-  if (c < chunks) {
-    if (poisoned) {
-#pragma unroll
-      for (int i = 0; i < VW; ++i) acc[i] = __int_as_float(0x7FC00000);
-    }
-    if (VEC) {
-      Vec16<TY> q;
-      q.from_float(acc);
-      st_v4(out + t * H + c * VW, q.u);
-    } else {
-      out[t * H + c] = Dt<TY>::from_f(acc[0]);
-    }
-  }
+  combine_warp<TY, TW, VEC, false>(y, row_of_slot, w, t, H, k, gw - t * warps_per_token, out,
+                                   lane);
 }
 
 template <typename TY, typename TW>

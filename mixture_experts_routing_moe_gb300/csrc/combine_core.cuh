@@ -1,0 +1,68 @@
+// One warp's share of the combine (ruDNN user guide, §3 "MoE-Workflow" / §6 "MoE aufrufen"):
+// columns [32 c0 VW, 32 c0 VW + 32 VW) of out[t] = sum_j w[t, j] * y[row_of_slot[t*k + j]],
+// FP32 accumulation in the fixed slot order j = 0..k-1, one rounding to the output dtype.  A
+// slot without a row (poisoned routing) makes the token's output NaN.  COHERENT reads y, the map
+// and the weights through L2 only (they were written earlier in the same launch).
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+template <typename TY, typename TW, bool VEC, bool COHERENT>
+__device__ __forceinline__ void combine_warp(const TY* __restrict__ y,
+                                             const uint32_t* __restrict__ row_of_slot,
+                                             const TW* __restrict__ w, int64_t t, int64_t H, int k,
+                                             int64_t c0, TY* __restrict__ out, int lane) {
+  constexpr int VW = VEC ? 16 / (int)sizeof(TY) : 1;
+  const int64_t chunks = H / VW;
+  const int64_t c = c0 * 32 + lane;  // this lane's column chunk
+  float acc[VW];
+#pragma unroll
+  for (int i = 0; i < VW; ++i) acc[i] = 0.f;
+  bool poisoned = false;
+  for (int jb = 0; jb < k; jb += 32) {
+    uint32_t my_row = kInvalidRow;
+    float my_w = 0.f;
+    if (jb + lane < k) {
+      my_row = ld_elem<COHERENT>(row_of_slot + t * k + jb + lane);
+      my_w = Dt<TW>::to_f(ld_elem<COHERENT>(w + t * k + jb + lane));
+    }
+    const int nj = min(32, k - jb);
+    for (int jj = 0; jj < nj; ++jj) {
+      const uint32_t r = __shfl_sync(0xFFFFFFFFu, my_row, jj);
+      const float wj = __shfl_sync(0xFFFFFFFFu, my_w, jj);
+      if (r == kInvalidRow) {
+        poisoned = true;
+        continue;
+      }
+      if (c < chunks) {
+        if (VEC) {
+          Vec16<TY> q;
+          q.u = ld_v4<COHERENT>(y + (int64_t)r * H + c * VW);
+          float f[VW];
+          q.to_float(f);
+#pragma unroll
+          for (int i = 0; i < VW; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+        } else {
+          acc[0] = fmaf(wj, Dt<TY>::to_f(ld_elem<COHERENT>(y + (int64_t)r * H + c)), acc[0]);
+        }
+      }
+    }
+  }
+  if (c < chunks) {
+    if (poisoned) {
+#pragma unroll
+      for (int i = 0; i < VW; ++i) acc[i] = __int_as_float(0x7FC00000);
+    }
+    if (VEC) {
+      Vec16<TY> q;
+      q.from_float(acc);
+      st_v4(out + t * H + c * VW, q.u);
+    } else {
+      out[t * H + c] = Dt<TY>::from_f(acc[0]);
+    }
+  }
+}
+
+}  // namespace moe

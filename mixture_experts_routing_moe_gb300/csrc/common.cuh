@@ -69,4 +69,44 @@ __device__ inline void st_cs_v4(void* p, uint4 v) {
                : "memory");
 }
 
+// Loads cached in L2 only: coherent with stores that other CTAs of the same launch made visible
+// (through a fence and a grid barrier) before this thread loads; never served from a stale L1.
+__device__ inline uint4 ld_cg_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p)
+               : "memory");
+  return r;
+}
+__device__ inline uint32_t ld_cg_u32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(r) : "l"(p) : "memory");
+  return r;
+}
+__device__ inline uint16_t ld_cg_u16(const void* p) {
+  uint16_t r;
+  asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(r) : "l"(p) : "memory");
+  return r;
+}
+// One element of type T; COHERENT selects an L2-only load over the read-only (nc) path.
+template <bool COHERENT, typename T>
+__device__ inline T ld_elem(const T* p) {
+  if constexpr (!COHERENT) {
+    return __ldg(p);
+  } else if constexpr (sizeof(T) == 4) {
+    const uint32_t u = ld_cg_u32(p);
+    return *reinterpret_cast<const T*>(&u);
+  } else {
+    static_assert(sizeof(T) == 2, "2- or 4-byte elements");
+    const uint16_t u = ld_cg_u16(p);
+    return *reinterpret_cast<const T*>(&u);
+  }
+}
+template <bool COHERENT>
+__device__ inline uint4 ld_v4(const void* p) {
+  if constexpr (COHERENT) return ld_cg_v4(p);
+  else return ld_nc_v4(p);
+}
+
 }  // namespace moe

@@ -20,6 +20,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "dispatch_core.cuh"
 #include "launch.h"
 
 // Scratch of moe_dispatch_static(): a status word (in the first 256 bytes) followed by the
@@ -166,80 +167,8 @@ __global__ void __launch_bounds__(kSmallWarps * 32)
                        int32_t* __restrict__ offsets, uint32_t* __restrict__ token_of_row,
                        uint32_t* __restrict__ row_of_slot, unsigned* status) {
   extern __shared__ int32_t small_smem[];
-  int32_t* hist = small_smem;                         // [kSmallWarps][E]
-  int32_t* off = small_smem + kSmallWarps * E;        // [E + 1]
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < kSmallWarps * E; i += blockDim.x) hist[i] = 0;
-  __syncthreads();
-  const int64_t s0 = (int64_t)warp * CH, s1 = (R < s0 + CH) ? R : s0 + CH;
-  int32_t* h = hist + warp * E;
-  bool bad = false;
-  for (int64_t base = s0; base < s1; base += 32) {
-    const int64_t s = base + lane;
-    const bool act = s < s1;
-    const uint32_t e = act ? idx[s] : 0xFFFFFFFFu;
-    const bool valid = act && e < (uint32_t)E;
-    bad |= act && !valid;
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : 0xFFFFFFFFu);
-    if (valid && lane == __ffs(peers) - 1) h[e] += __popc(peers);
-    __syncwarp();
-  }
-  if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(status, kStatusIndex);
-  __syncthreads();
-  // per expert: exclusive prefix over the chunks, and the expert's total
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int32_t run = 0;
-    for (int w = 0; w < kSmallWarps; ++w) {
-      const int32_t c = hist[w * E + e];
-      hist[w * E + e] = run;
-      run += c;
-    }
-    off[e] = run;
-  }
-  __syncthreads();
-  if (warp == 0) {  // exclusive scan of the totals -> offsets
-    int32_t carry = 0;
-    for (int b = 0; b < E; b += 32) {
-      const int e = b + lane;
-      const int32_t c = e < E ? off[e] : 0;
-      int32_t x = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int32_t y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-        if (lane >= o) x += y;
-      }
-      if (e < E) {
-        off[e] = carry + x - c;
-        offsets[e] = carry + x - c;
-      }
-      carry += __shfl_sync(0xFFFFFFFFu, x, 31);
-    }
-    if (lane == 0) {
-      off[E] = carry;
-      offsets[E] = carry;
-    }
-  }
-  __syncthreads();
-  for (int e = lane; e < E; e += 32) h[e] += off[e];  // running row of each expert in this chunk
-  __syncwarp();
-  const unsigned lt = (1u << lane) - 1u;
-  for (int64_t base = s0; base < s1; base += 32) {
-    const int64_t s = base + lane;
-    const bool act = s < s1;
-    const uint32_t e = act ? idx[s] : 0xFFFFFFFFu;
-    const bool valid = act && e < (uint32_t)E;
-    const unsigned peers = __match_any_sync(0xFFFFFFFFu, valid ? e : 0xFFFFFFFFu);
-    if (valid) {
-      const uint32_t row = (uint32_t)(h[e] + __popc(peers & lt));
-      row_of_slot[s] = row;
-      token_of_row[row] = (uint32_t)(s / k);
-    } else if (act) {
-      row_of_slot[s] = kInvalidRow;
-    }
-    __syncwarp();
-    if (valid && lane == __ffs(peers) - 1) h[e] += __popc(peers);
-    __syncwarp();
-  }
+  dispatch_block<false>(idx, R, E, k, kSmallWarps, CH, small_smem, small_smem + kSmallWarps * E,
+                        offsets, token_of_row, row_of_slot, status);
 }
 
 // One block per token (grid-stride): x[t] is read once and written to its k dispatched rows.

@@ -4,9 +4,10 @@
 //   kernel down:     y[r, h] = a[r] . down[e, h]                                   (y stored in wdt)
 // over the ragged row groups offsets[e] .. offsets[e+1]-1 of the dispatched rows.
 //
-// Two variants share the structure below: a CTA kernel (one 128 x 256 tile per CTA) and a
-// CTA-pair kernel (one 256 x 256 tile per cluster of two CTAs, cta_group::2, see further down);
-// the launcher takes the pair when experts average at least 128 rows.
+// Two variants share the structure below: a CTA kernel (one 128 x 256 tile per CTA, its warp
+// roles in gemm_cta.cuh) and a CTA-pair kernel (one 256 x 256 tile per cluster of two CTAs,
+// cta_group::2, see further down); the launcher takes the pair when experts average at least 128
+// rows.
 // Both kernels are persistent (one CTA per SM) with three warp roles:
 //   warp 0     TMA producer: per 64-deep K slice loads a 128-row A tile (x_d or a) and a
 //              256-row B tile into a 4-stage shared-memory ring (128-byte swizzle).  For
@@ -26,6 +27,7 @@
 #include <cuda.h>
 
 #include "common.cuh"
+#include "gemm_cta.cuh"
 #include "launch.h"
 #include "tcgen05.cuh"
 #include "tiles.cuh"
@@ -33,58 +35,7 @@
 namespace moe {
 namespace {
 using namespace tc;
-
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;
-constexpr int kMaxExperts = 1024;
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_BYTES +
-                              256 /*barriers, flags*/ + (kMaxExperts + 4) * sizeof(int);
-
-// Tile t -> (expert e, m-tile m, n-tile n).  Inside an expert, the operand with fewer bytes
-// (A: mt * 128 rows, B: NT * 256 rows, both K deep) is the one kept resident in L2 while the
-// other streams through once: A resident -> n outer, m inner; B resident -> m outer, n inner.
-// When the resident operand exceeds kResidentBytes it is cut into groups that do fit.
-// Returns true when A is the resident operand.
-constexpr long long kResidentBytes = 64ll << 20;
-template <int TBM = BM>
-__device__ __forceinline__ bool decode_tile(int t, const int* pref, int E, int NT, int K, int& e,
-                                            int& m, int& n) {
-  e = find_expert(pref, E, t / NT);
-  const int local = t - pref[e] * NT;
-  const int mt = pref[e + 1] - pref[e];
-  const long long rows_fit = kResidentBytes / ((long long)K * 2);
-  if ((long long)mt * TBM <= (long long)NT * BN) {
-    const int g = (int)max(1ll, min((long long)mt, rows_fit / TBM));
-    const int grp = local / (g * NT);
-    const int gm = min(g, mt - grp * g);
-    const int r = local - grp * g * NT;
-    n = r / gm;
-    m = grp * g + r % gm;
-    return true;
-  }
-  const int g = (int)max(1ll, min((long long)NT, rows_fit / BN));
-  const int grp = local / (g * mt);
-  const int gn = min(g, NT - grp * g);
-  const int r = local - grp * g * mt;
-  m = r / gn;
-  n = grp * g + r % gn;
-  return false;
-}
-
-struct TcParams {
-  const int32_t* offsets;
-  uint8_t* out;       // a [rows, N] (gate/up) or y [rows, N] (down), 16-bit elements
-  unsigned* status;
-  int E;
-  int N;              // valid output columns: I (gate/up) or H (down)
-  int KB;             // 64-deep K slices: ceil(H / 64) or ceil(I / 64)
-  int NT;             // n-tiles per expert: ceil(I / 128) or ceil(H / 256)
-  int b_rows;         // rows of the B tensor per expert: I or H
-};
+using namespace cta_gemm;
 
 template <bool GATEUP, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -92,34 +43,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap mapB0,
                    const __grid_constant__ CUtensorMap mapB1, const TcParams p) {
   extern __shared__ uint8_t tc_smem_raw[];
-  const uint32_t raw = smem_u32(tc_smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = tc_smem_raw + (base - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * STAGE_BYTES);
-  const uint32_t bar0 = smem_u32(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
-  volatile int* abort_f = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* pref = reinterpret_cast<int*>(tmem_slot + 4);
-
+  uint32_t* tmem_slot;
+  int* pref;
+  Ring ring = carve_ring(tc_smem_raw, &tmem_slot, &pref);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
-    }
-    mbar_init(drain_bar, 1);
-    *abort_f = 0;
-    fence_mbar_init();
-  }
+  if (threadIdx.x == 0) init_ring(ring);
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   if (warp == 2) build_mtile_prefix(p.offsets, p.E, BM, pref, lane);
   if (warp == 0 && lane == 0) {
@@ -130,172 +58,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  const int total = pref[p.E] * p.NT;
+  ring.tmem_base = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
-      // ------------------------------------------------------------ TMA producer
-      int stage = 0, armed = 0;
-      uint32_t phase = 0;
-      bool stop = false;
-      // The resident operand is marked evict_last.  The other one is NOT marked evict_first:
-      // each of its tiles is still read by every CTA of the same m-row / n-column, shortly apart.
-      const uint64_t keep = policy_evict_last(), other = policy_evict_normal();
-      for (int t = blockIdx.x; t < total && !stop; t += gridDim.x) {
-        int e, m, n;
-        const bool a_res = decode_tile(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
-        const uint64_t pa = a_res ? keep : other, pb = a_res ? other : keep;
-        const int a_row = __ldg(p.offsets + e) + m * BM;
-        const int b_row = e * p.b_rows + n * (GATEUP ? BN / 2 : BN);
-        for (int kb = 0; kb < p.KB; ++kb) {
-          if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_f, p.status)) {
-            stop = true;
-            break;
-          }
-          const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
-          mbar_expect_tx(full_bar(stage), STAGE_BYTES);
-          tma_load_2d(sa, &mapA, full_bar(stage), kb * BK, a_row, pa);
-          if (GATEUP) {
-            tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, b_row, pb);
-            tma_load_2d(sb + B_BYTES / 2, &mapB1, full_bar(stage), kb * BK, b_row, pb);
-          } else {
-            tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, b_row, pb);
-          }
-          ++armed;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (*abort_f) {  // let the copies still in flight land before the CTA exits
-        for (int i = 0; i < min(armed, STAGES); ++i) {
-          if (stage == 0) {
-            stage = STAGES - 1;
-            phase ^= 1u;
-          } else {
-            --stage;
-          }
-          wait_drain(full_bar(stage), phase);
-        }
-      }
+      ProducerState st;
+      producer<GATEUP, false>(&mapA, &mapB0, &mapB1, p, pref, ring, st);
+      if (*ring.abort_f) producer_drain(ring, st);  // any role gave up: let copies land
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = make_idesc(BF16, BM, BN);
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      bool stop = false;
-      for (int t = blockIdx.x; t < total && !stop; t += gridDim.x) {
-        if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_f, p.status)) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < p.KB; ++kb) {
-          if (!wait_bounded(full_bar(stage), phase, abort_f, p.status)) {
-            stop = true;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
-          const uint64_t da = make_sdesc(sa), db = make_sdesc(sb);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 elements = 32 bytes along K
-            umma_f16(d_tmem, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
-          umma_commit(empty_bar(stage));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (stop) break;
-        umma_commit(tfull_bar(acc));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
-      }
-      umma_commit(drain_bar);  // arrives once every MMA issued above has completed
-      wait_drain(drain_bar, 0);
+      MmaState st;
+      mma<BF16>(p, pref, ring, st);
+      mma_drain(ring);
     }
   } else {
-    // -------------------------------------------------------------- epilogue (warps 2..5)
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      int e, m, n;
-      decode_tile(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
-      const bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_f, p.status);
-      if (!__all_sync(0xFFFFFFFFu, ok)) break;
-      tc_fence_after();
-      const int row = __ldg(p.offsets + e) + m * BM + q * 32 + lane;
-      const bool valid = row < __ldg(p.offsets + e + 1);
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      uint8_t* orow = p.out + (size_t)row * p.N * 2;
-      if (GATEUP) {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t g[32], u[32];
-          tmem_ld32(taddr + c * 32, g);
-          tmem_ld32(taddr + BN / 2 + c * 32, u);
-          tmem_wait_ld();
-          const int col0 = n * (BN / 2) + c * 32;
-          if (valid) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              if (col0 + v * 8 < p.N) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  float a2[2];
-#pragma unroll
-                  for (int h = 0; h < 2; ++h) {
-                    const float gv = __uint_as_float(g[v * 8 + i * 2 + h]);
-                    const float uv = __uint_as_float(u[v * 8 + i * 2 + h]);
-                    a2[h] = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
-                  }
-                  pk[i] = pack2<BF16>(a2[0], a2[1]);
-                }
-                st_v4(orow + (size_t)(col0 + v * 8) * 2, make_uint4(pk[0], pk[1], pk[2], pk[3]));
-              }
-            }
-          }
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c * 32, r);
-          tmem_wait_ld();
-          const int col0 = n * BN + c * 32;
-          if (valid) {
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              if (col0 + v * 8 < p.N) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  pk[i] = pack2<BF16>(__uint_as_float(r[v * 8 + i * 2]),
-                                      __uint_as_float(r[v * 8 + i * 2 + 1]));
-                st_v4(orow + (size_t)(col0 + v * 8) * 2, make_uint4(pk[0], pk[1], pk[2], pk[3]));
-              }
-            }
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1u;
-    }
+    EpilogueState st;
+    epilogue<GATEUP, BF16, false>(p, pref, ring, st, warp, lane);
   }
 
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc(ring.tmem_base, kTmemCols);
   }
 }
 

@@ -72,6 +72,32 @@ cudaError_t launch_experts_simt(const float* x_d, const int32_t* offsets, int64_
                                 int H, int I, float* y, float* a, cudaStream_t s,
                                 cudaEvent_t between = nullptr);
 
+// Fused forward of short batches (route, dispatch, gate/up, down, combine in one cooperative
+// launch).  fused_decode_supported() says whether moe_forward takes it for a shape; pointer
+// alignment (16 bytes) is checked by the caller.  grid_count must be zero at launch.
+constexpr int kFusedDecodeMaxExperts = 256;
+constexpr int64_t kFusedDecodeMaxRows = 4096;
+struct FusedDecodeArgs {
+  const void* logits;
+  const void* x;
+  const void* gate;
+  const void* up;
+  const void* down;
+  int64_t T;
+  int E, H, I, k, renorm;
+  uint32_t* idx;
+  void* w;
+  uint32_t* row_of_slot;
+  int32_t* offsets;
+  void* x_d;
+  void* a;
+  void* out;
+  unsigned* status;
+  unsigned* grid_count;
+};
+bool fused_decode_supported(int64_t T, int E, int64_t H, int64_t I, int k, int ldt, int wdt);
+cudaError_t launch_decode_fused(const FusedDecodeArgs& f, int ldt, int wdt, cudaStream_t s);
+
 // bf16 / f16 experts on tcgen05 tensor cores; `a` is an [rows, I] scratch buffer of dtype wdt.
 cudaError_t launch_experts_tc(const void* x_d, const int32_t* offsets, int64_t rows,
                               const void* gate, const void* up, const void* down, int wdt, int E,

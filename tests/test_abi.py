@@ -22,7 +22,7 @@ F32, F16, BF16 = B.MOE_F32, B.MOE_F16, B.MOE_BF16
 
 def test_exports_every_header_function(L):
     names = B.header_functions()
-    assert len(names) == 21
+    assert len(names) == 22
     for n in names:
         assert hasattr(L, n), n
     assert L.moe_abi_version() == 1
