@@ -29,8 +29,10 @@ struct Cursor {
 };
 
 struct FwdLayout {
-  size_t idx, w, ros, tor, offsets, hist, xd, a, total;
+  size_t idx, w, ros, tor, offsets, hist, ready, xd, a, total;
 };
+size_t ready_bytes(int64_t R, int64_t E) { return (size_t)((R + 127) / 128 + E + 1) * 4; }
+
 FwdLayout fwd_layout(int64_t T, int64_t E, int64_t H, int64_t I, int k, int ldt, int wdt) {
   const int64_t R = T * k;
   FwdLayout l;
@@ -42,6 +44,7 @@ FwdLayout fwd_layout(int64_t T, int64_t E, int64_t H, int64_t I, int k, int ldt,
   l.tor = c.take((size_t)R * 4);
   l.offsets = c.take((size_t)(E + 1) * 4);
   l.hist = c.take(dispatch_scratch_bytes(R, (int)E));
+  l.ready = c.take(ready_bytes(R, E));  // per-m-tile counters of the fused short-batch path
   l.xd = c.take((size_t)R * H * dtype_size(wdt));  // x_d, later reused for y
   l.a = c.take((size_t)R * I * dtype_size(wdt));
   l.total = c.off;
@@ -156,7 +159,8 @@ int run_forward(const void* x, const void* logits, int ldt, const void* gate, co
 
   if (allow_fused && !events && aligned16(logits) &&
       takes_fused(rs, T, E, H, I, top_k, ldt, wdt)) {
-    // status word at byte 0 and the grid-barrier counter at byte 64 of the header, both zeroed
+    // status word at byte 0 and grid-barrier counter at byte 64 of the header zeroed here; the
+    // tile counter (byte 128) and the per-m-tile counters are zeroed by the kernel
     if (cudaMemsetAsync(ws, 0, 128, s) != cudaSuccess) return MOE_ERR_CUDA;
     FusedDecodeArgs f{};
     f.logits = logits;
@@ -179,6 +183,8 @@ int run_forward(const void* x, const void* logits, int ldt, const void* gate, co
     f.out = out;
     f.status = status;
     f.grid_count = (unsigned*)(b + 64);
+    f.tile_count = (unsigned*)(b + 128);
+    f.mtile_ready = (unsigned*)(b + L.ready);
     return cuda_status(launch_decode_fused(f, ldt, wdt, s));
   }
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return MOE_ERR_CUDA;

@@ -29,23 +29,44 @@ __device__ __forceinline__ void combine_warp(const TY* __restrict__ y,
       my_w = Dt<TW>::to_f(ld_elem<COHERENT>(w + t * k + jb + lane));
     }
     const int nj = min(32, k - jb);
-    for (int jj = 0; jj < nj; ++jj) {
-      const uint32_t r = __shfl_sync(0xFFFFFFFFu, my_row, jj);
-      const float wj = __shfl_sync(0xFFFFFFFFu, my_w, jj);
-      if (r == kInvalidRow) {
-        poisoned = true;
-        continue;
-      }
-      if (c < chunks) {
-        if (VEC) {
-          Vec16<TY> q;
-          q.u = ld_v4<COHERENT>(y + (int64_t)r * H + c * VW);
-          float f[VW];
-          q.to_float(f);
+    // groups of kBatch slots: all loads of a group are issued before its FMAs, which still run
+    // in slot order
+    constexpr int kBatch = 8;
+    for (int j0 = 0; j0 < nj; j0 += kBatch) {
+      uint32_t r[kBatch];
+      float wj[kBatch];
+      uint4 v[kBatch];
 #pragma unroll
-          for (int i = 0; i < VW; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+      for (int b = 0; b < kBatch; ++b) {
+        const int jj = min(j0 + b, nj - 1);
+        r[b] = __shfl_sync(0xFFFFFFFFu, my_row, jj);
+        wj[b] = __shfl_sync(0xFFFFFFFFu, my_w, jj);
+        const bool live = j0 + b < nj && r[b] != kInvalidRow && c < chunks;
+        if (VEC) {
+          v[b] = live ? ld_v4<COHERENT>(y + (int64_t)r[b] * H + c * VW) : make_uint4(0, 0, 0, 0);
         } else {
-          acc[0] = fmaf(wj, Dt<TY>::to_f(ld_elem<COHERENT>(y + (int64_t)r * H + c)), acc[0]);
+          const float f = live ? Dt<TY>::to_f(ld_elem<COHERENT>(y + (int64_t)r[b] * H + c)) : 0.f;
+          v[b].x = __float_as_uint(f);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        if (j0 + b >= nj) break;
+        if (r[b] == kInvalidRow) {
+          poisoned = true;
+          continue;
+        }
+        if (c < chunks) {
+          if (VEC) {
+            Vec16<TY> q;
+            q.u = v[b];
+            float f[VW];
+            q.to_float(f);
+#pragma unroll
+            for (int i = 0; i < VW; ++i) acc[i] = fmaf(wj[b], f[i], acc[i]);
+          } else {
+            acc[0] = fmaf(wj[b], __uint_as_float(v[b].x), acc[0]);
+          }
         }
       }
     }

@@ -13,7 +13,9 @@
 //                stable order as the dispatch kernels); CTA 0 publishes offsets and row_of_slot;
 //                each CTA gathers its contiguous share of the rows of x_d.
 //   3. gate/up   the single-CTA tcgen05 GEMM over the tile list of the offsets -> a.
-//   4. down      the same GEMM on a -> y (y reuses the x_d buffer).
+//   4. down      the same GEMM on a -> y (y reuses the x_d buffer).  No barrier before it: a
+//                per-m-tile count of stored gate/up warps gates the A loads of each down tile,
+//                so the down GEMM starts while the last gate/up tiles are still running.
 //   5. combine   (token, 256-column chunk) items strided over all warps (combine_core.cuh).
 // Data written in one phase and read in a later one goes through L2 only: generic loads use
 // ld.global.cg, and x_d / a, which the next phase reads with TMA, are ordered for the async proxy
@@ -39,11 +41,24 @@ using namespace cta_gemm;
 
 constexpr int kWarps = kThreads / 32;
 constexpr int kOffInts = kFusedDecodeMaxExperts + 8;  // persistent copy of the offsets
-constexpr size_t kFusedSmemBytes = kSmemBytes + kOffInts * sizeof(int);
+// Tile ring of the dynamic scheduler: ids of the next tiles, claimed by the producer from a
+// global counter and read in order by the MMA thread and the four epilogue warps.
+constexpr int kTileSlots = 4;
+constexpr int kSchedBytes = 2 * kTileSlots * 8 + kTileSlots * 4 + 16;
+constexpr size_t kFusedSmemBytes = kSmemBytes + kOffInts * sizeof(int) + kSchedBytes;
+
+struct TileRing {
+  uint32_t bar0;      // full[0..3] then empty[0..3]
+  volatile int* ids;  // [kTileSlots]; -1 = no more tiles
+  __device__ uint32_t full(int q) const { return bar0 + 8u * q; }
+  __device__ uint32_t empty(int q) const { return bar0 + 8u * (kTileSlots + q); }
+};
 
 struct DecodeParams {
   const void* logits;
   const void* x;
+  const void* gate;       // [E, I, H]
+  const void* up;         // [E, I, H]
   int T, E, H, I, k, renorm;
   uint32_t* idx;          // [T k]
   void* w;                // [T k] in the logits dtype
@@ -54,17 +69,12 @@ struct DecodeParams {
   void* out;              // [T, H]
   unsigned* status;
   unsigned* grid_count;   // zero at launch
+  unsigned* tile_count;   // zeroed in phase 1: GEMM tiles claimed after the static first ones
+  unsigned* mtile_ready;  // [n_ready], zeroed in phase 1: stored gate/up warps per m-tile
+  int n_ready;
   TcParams gu, dn;        // offsets filled in by the kernel (shared memory)
 };
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
 // Generic-proxy writes of this thread (global and shared) before later async-proxy accesses.
 __device__ __forceinline__ void fence_proxy_async_all() {
   asm volatile("fence.proxy.async;" ::: "memory");
@@ -80,7 +90,7 @@ __device__ __forceinline__ void grid_barrier(unsigned* count, unsigned n, volati
     atomicAdd(count, 1u);
     const unsigned target = n * gridDim.x;
     const long long t0 = clock64();
-    while (ld_acquire_gpu(count) < target) {
+    while (ld_acquire_gpu_u32(count) < target) {
       if (clock64() - t0 > kWaitLimit) {
         *abort_f = 1;
         atomicOr(status, kStatusTimeout);
@@ -106,12 +116,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* pref;
   Ring ring = carve_ring(fd_smem_raw, &tmem_slot, &pref);
   int32_t* offs = reinterpret_cast<int32_t*>(pref + kMaxExperts + 4);
+  TileRing tr;
+  int* first_tile;  // the first GEMM tile this CTA claimed (-1: none)
+  {
+    uint64_t* b = reinterpret_cast<uint64_t*>(offs + kOffInts);  // 8-byte aligned: kOffInts even
+    tr.bar0 = smem_u32(b);
+    tr.ids = reinterpret_cast<volatile int*>(b + 2 * kTileSlots);
+    first_tile = const_cast<int*>(tr.ids + kTileSlots);
+  }
   // the stage ring doubles as scratch for the phases that run before and after the GEMMs
   uint8_t* scratch = fd_smem_raw + (ring.base - smem_u32(fd_smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t R = (int64_t)p.T * p.k;
 
-  if (threadIdx.x == 0) init_ring(ring);
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < kTileSlots; ++q) {
+      mbar_init(tr.full(q), 1);
+      mbar_init(tr.empty(q), 1 + 4);  // the MMA thread and the four epilogue warps
+    }
+    init_ring(ring);  // also fences the barrier initialisation
+  }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   if (warp == 0 && lane == 0) {
     tma_prefetch(&map_xd);
@@ -129,6 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   EpilogueState est;
 
   // ---------------------------------------------------------------- 1. route
+  if (blockIdx.x == 0) {  // counters first used after barrier 2: zeroed here, not by the host
+    if (threadIdx.x == 0) *p.tile_count = 0u;
+    for (int i = threadIdx.x; i < p.n_ready; i += blockDim.x) p.mtile_ready[i] = 0u;
+  }
   {
     uint32_t* s_id = reinterpret_cast<uint32_t*>(scratch) + warp * p.k;
     float* s_e = reinterpret_cast<float*>(scratch + (size_t)kWarps * p.k * 4) + warp * p.k;
@@ -145,55 +173,150 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!*ring.abort_f) {
     int32_t* hist = reinterpret_cast<int32_t*>(scratch);  // [kWarps][E]
     int32_t* off_s = hist + kWarps * p.E;                  // [E + 1]
-    uint32_t* tor = reinterpret_cast<uint32_t*>(off_s + p.E + 8);
+    uint32_t* tor = reinterpret_cast<uint32_t*>(off_s + p.E + 8);  // [R]
+    uint32_t* idx_s = reinterpret_cast<uint32_t*>(                  // [R], 16-byte aligned
+        (reinterpret_cast<uintptr_t>(tor + R) + 15) & ~static_cast<uintptr_t>(15));
+    // all ids into shared memory first: one round trip to L2 instead of one per 32 slots
+    for (int64_t i = threadIdx.x; i < (R + 3) / 4; i += blockDim.x) {
+      if (4 * i + 3 < R) {
+        *reinterpret_cast<uint4*>(idx_s + 4 * i) = ld_cg_v4(p.idx + 4 * i);
+      } else {
+        for (int64_t j = 4 * i; j < R; ++j) idx_s[j] = ld_cg_u32(p.idx + j);
+      }
+    }
+    __syncthreads();
     const int CH = (int)(((R + kWarps - 1) / kWarps + 31) / 32 * 32);
     const bool lead = blockIdx.x == 0;
-    dispatch_block<true>(p.idx, R, p.E, p.k, kWarps, CH, hist, off_s, lead ? p.offsets : nullptr,
-                         tor, lead ? p.row_of_slot : nullptr, lead ? p.status : nullptr);
-    __syncthreads();
+    dispatch_count<true>(idx_s, R, p.E, kWarps, CH, hist, off_s, lead ? p.offsets : nullptr,
+                         lead ? p.status : nullptr);
     for (int e = threadIdx.x; e <= p.E; e += blockDim.x) offs[e] = off_s[e];
+    __syncthreads();
+    if (warp == 2) build_mtile_prefix(offs, p.E, BM, pref, lane);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      // The tile list is known now.  This CTA's first GEMM tile is tile blockIdx.x (static, so
+      // no contention on the claim counter); half of its gate and up rows (contiguous in memory)
+      // go to L2 while the slots are scattered and the rows of x_d gathered.  Over the grid
+      // that is at most 152 x 2 x 64 rows x H x 2 bytes: 78 MB at H = 2048, within L2.
+      const int n_gu = pref[p.E] * p.gu.NT;
+      const int n_dn = pref[p.E] * p.dn.NT;
+      int t = (int)blockIdx.x;
+      if (t >= n_gu + n_dn) t = -1;
+      *first_tile = t;
+      if (t >= 0 && t < n_gu) {
+        int e, m, n;
+        decode_tile(t, pref, p.E, p.gu.NT, p.gu.KB * BK, e, m, n);
+        const int rows = min(64, p.I - n * (BN / 2));
+        const size_t row0 = (size_t)e * p.I + n * (BN / 2);
+        const uint32_t bytes = (uint32_t)rows * p.H * 2;
+        bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.gate) + row0 * p.H * 2, bytes);
+        bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.up) + row0 * p.H * 2, bytes);
+      }
+    }
+    dispatch_scatter<true>(idx_s, R, p.E, p.k, CH, hist, tor, lead ? p.row_of_slot : nullptr);
+    __syncthreads();
     // rows [r0, r1) of x_d: x_d[r] = x[token_of_row[r]], 16-byte vectors
-    const int64_t per = (R + gridDim.x - 1) / gridDim.x;
-    const int64_t r0 = min(R, (int64_t)blockIdx.x * per), r1 = min(R, r0 + per);
-    const int64_t vec_per_row = (int64_t)p.H * 2 / 16;
+    // 32-bit index arithmetic: R <= 4096 rows of H / 8 <= 2^16 vectors (64-bit division is slow)
+    const uint32_t per = (uint32_t)((R + gridDim.x - 1) / gridDim.x);
+    const uint32_t r0 = min((uint32_t)R, blockIdx.x * per), r1 = min((uint32_t)R, r0 + per);
+    const uint32_t vpr = (uint32_t)p.H / 8;  // 16-byte vectors per row
     const uint4* xs = reinterpret_cast<const uint4*>(p.x);
     uint4* xd = reinterpret_cast<uint4*>(p.x_d);
-    for (int64_t i = threadIdx.x; i < (r1 - r0) * vec_per_row; i += blockDim.x) {
-      const int64_t r = r0 + i / vec_per_row, c = i % vec_per_row;
-      st_v4(xd + r * vec_per_row + c, ld_nc_v4(xs + (int64_t)tor[r] * vec_per_row + c));
+    const uint32_t nvec = (r1 - r0) * vpr;
+    constexpr int kInFlight = 8;  // 16-byte loads issued before their stores
+    for (uint32_t i0 = threadIdx.x; i0 < nvec; i0 += blockDim.x * kInFlight) {
+      uint4 v[kInFlight];
+      uint32_t dst[kInFlight];
+#pragma unroll
+      for (int b = 0; b < kInFlight; ++b) {
+        const uint32_t i = i0 + b * blockDim.x;
+        if (i < nvec) {
+          const uint32_t rr = i / vpr, c = i - rr * vpr;
+          dst[b] = (r0 + rr) * vpr + c;
+          v[b] = ld_nc_v4(xs + (size_t)tor[r0 + rr] * vpr + c);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kInFlight; ++b)
+        if (i0 + b * blockDim.x < nvec) st_v4(xd + dst[b], v[b]);
     }
     // x_d is read by TMA after the barrier, and TMA refills this scratch shared memory
     fence_proxy_async_all();
-    __syncthreads();
-    if (warp == 2) build_mtile_prefix(offs, p.E, BM, pref, lane);
   }
   grid_barrier(p.grid_count, 2, ring.abort_f, p.status);
 
   // ---------------------------------------------------------------- 3. gate/up, 4. down
-  TcParams gu = p.gu, dn = p.dn;
-  gu.offsets = offs;
-  dn.offsets = offs;
-  for (int g = 0; g < 2 && !*ring.abort_f; ++g) {
-    const TcParams& tp = g == 0 ? gu : dn;
+  // One tile list: the gate/up tiles, then the down tiles, claimed dynamically (a global counter)
+  // so that CTAs finish together.  No grid barrier between the GEMMs: the gate/up epilogue counts
+  // the stored warps of every m-tile, and the down producer loads the A rows (a) of an m-tile
+  // only once all 4 NT_gu warps of it have stored.  Every gate/up tile is claimed before any down
+  // tile and its CTA completes it without waiting on anything, so every wait ends.
+  if (!*ring.abort_f) {
+    TcParams gu = p.gu, dn = p.dn;
+    gu.offsets = offs;
+    dn.offsets = offs;
+    gu.ready_signal = p.mtile_ready;
+    dn.ready_wait = p.mtile_ready;
+    dn.ready_target = 4u * (unsigned)gu.NT;
+    const int n_gu = pref[p.E] * gu.NT, total = n_gu + pref[p.E] * dn.NT;
+    int q = 0;
+    uint32_t ph = 0;
     if (warp == 0) {
       if (lane == 0) {
         fence_proxy_async_global();
-        if (g == 0)
-          producer<true, true>(&map_xd, &map_gate, &map_up, tp, pref, ring, pst);
-        else
-          producer<false, true>(&map_a, &map_down, &map_down, tp, pref, ring, pst);
+        bool first = true;
+        while (wait_bounded(tr.empty(q), ph ^ 1u, ring.abort_f, p.status)) {
+          int t = first ? *first_tile : (int)(gridDim.x + atomicAdd(p.tile_count, 1u));
+          first = false;
+          if (t >= total) t = -1;
+          tr.ids[q] = t;
+          mbar_arrive(tr.full(q));
+          if (t < 0) break;
+          const bool ok =
+              t < n_gu
+                  ? producer_tile<true, true>(&map_xd, &map_gate, &map_up, gu, pref, ring, pst, t)
+                  : producer_tile<false, true>(&map_a, &map_down, &map_down, dn, pref, ring, pst,
+                                               t - n_gu);
+          if (!ok) break;
+          if (++q == kTileSlots) {
+            q = 0;
+            ph ^= 1u;
+          }
+        }
       }
     } else if (warp == 1) {
-      if (lane == 0) mma<BF16>(tp, pref, ring, mst);
+      if (lane == 0) {
+        while (wait_bounded(tr.full(q), ph, ring.abort_f, p.status)) {
+          const int t = tr.ids[q];
+          mbar_arrive(tr.empty(q));
+          if (t < 0 || !mma_tile<BF16>(t < n_gu ? gu : dn, ring, mst)) break;
+          if (++q == kTileSlots) {
+            q = 0;
+            ph ^= 1u;
+          }
+        }
+      }
     } else {
-      if (g == 0)
-        epilogue<true, BF16, true>(tp, pref, ring, est, warp, lane);
-      else
-        epilogue<false, BF16, true>(tp, pref, ring, est, warp, lane);
-      fence_proxy_async_global();  // a is read by TMA after the barrier
+      while (true) {
+        const bool ok = wait_bounded(tr.full(q), ph, ring.abort_f, p.status);
+        if (!__all_sync(0xFFFFFFFFu, ok)) break;
+        const int t = tr.ids[q];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tr.empty(q));
+        if (t < 0) break;
+        const bool done = t < n_gu
+                              ? epilogue_tile<true, BF16, true>(gu, pref, ring, est, t, warp, lane)
+                              : epilogue_tile<false, BF16, true>(dn, pref, ring, est, t - n_gu,
+                                                                 warp, lane);
+        if (!done) break;
+        if (++q == kTileSlots) {
+          q = 0;
+          ph ^= 1u;
+        }
+      }
     }
-    grid_barrier(p.grid_count, 3 + g, ring.abort_f, p.status);
   }
+  grid_barrier(p.grid_count, 3, ring.abort_f, p.status);
 
   // ---------------------------------------------------------------- 5. combine
   if (!*ring.abort_f) {
@@ -201,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t wpt = (chunks + 31) / 32;
     for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < (int64_t)p.T * wpt;
          it += (int64_t)gridDim.x * kWarps) {
-      const int64_t t = it / wpt;
+      const int64_t t = (uint32_t)it / (uint32_t)wpt;  // 32-bit division (it < T * wpt)
       combine_warp<TX, TL, true, true>(reinterpret_cast<const TX*>(p.x_d), p.row_of_slot,
                                        reinterpret_cast<const TL*>(p.w), t, p.H, p.k,
                                        it - t * wpt, reinterpret_cast<TX*>(p.out), lane);
@@ -247,6 +370,8 @@ cudaError_t launch_t(const FusedDecodeArgs& f, cudaStream_t s) {
   DecodeParams p{};
   p.logits = f.logits;
   p.x = f.x;
+  p.gate = f.gate;
+  p.up = f.up;
   p.T = (int)f.T;
   p.E = f.E;
   p.H = f.H;
@@ -262,6 +387,9 @@ cudaError_t launch_t(const FusedDecodeArgs& f, cudaStream_t s) {
   p.out = f.out;
   p.status = f.status;
   p.grid_count = f.grid_count;
+  p.tile_count = f.tile_count;
+  p.mtile_ready = f.mtile_ready;
+  p.n_ready = (int)((R + BM - 1) / BM + f.E + 1);
   p.gu.out = (uint8_t*)f.a;
   p.gu.status = f.status;
   p.gu.E = f.E;

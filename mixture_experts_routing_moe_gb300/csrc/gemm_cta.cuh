@@ -74,7 +74,43 @@ struct TcParams {
   int KB;                  // 64-deep K slices: ceil(H / 64) or ceil(I / 64)
   int NT;                  // n-tiles per expert: ceil(I / 128) or ceil(H / 256)
   int b_rows;              // rows of the B tensor per expert: I or H
+  // Dataflow between two GEMMs of one launch (null when unused).  ready_signal: the epilogue
+  // adds 1 per warp to ready_signal[global m-tile] once its rows of a tile are stored.
+  // ready_wait: before the first A load of a tile the producer waits until
+  // ready_wait[global m-tile] >= ready_target.  Global m-tile = pref[e] + m.
+  unsigned* ready_signal;
+  const unsigned* ready_wait;
+  unsigned ready_target;
 };
+
+__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Bounded wait until *cnt >= target (then the generic-proxy stores it counts are visible to TMA).
+__device__ __forceinline__ bool wait_count(const unsigned* cnt, unsigned target,
+                                           volatile int* abort_f, unsigned* status) {
+  if (ld_acquire_gpu_u32(cnt) >= target) {
+    fence_proxy_async_global();
+    return true;
+  }
+  const long long t0 = clock64();
+  while (ld_acquire_gpu_u32(cnt) < target) {
+    if (*abort_f) return false;
+    if (clock64() - t0 > kWaitLimit) {
+      *abort_f = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  fence_proxy_async_global();
+  return true;
+}
 
 // offsets[e]: read-only path for a standalone launch, a plain load when FUSED (shared memory).
 template <bool FUSED>
@@ -142,38 +178,51 @@ __device__ __forceinline__ void init_ring(const Ring& r) {
 }
 
 // ---------------------------------------------------------------- producer (one thread)
+// All K slices of tile t.
+template <bool GATEUP, bool FUSED>
+__device__ __forceinline__ bool producer_tile(const CUtensorMap* mapA, const CUtensorMap* mapB0,
+                                              const CUtensorMap* mapB1, const TcParams& p,
+                                              const int* pref, const Ring& r, ProducerState& st,
+                                              int t) {
+  // The resident operand is marked evict_last.  The other one is NOT marked evict_first:
+  // each of its tiles is still read by every CTA of the same m-row / n-column, shortly apart.
+  const uint64_t keep = policy_evict_last(), other = policy_evict_normal();
+  int e, m, n;
+  const bool a_res = decode_tile(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
+  const uint64_t pa = a_res ? keep : other, pb = a_res ? other : keep;
+  const int a_row = off_at<FUSED>(p.offsets, e) + m * BM;
+  const int b_row = e * p.b_rows + n * (GATEUP ? BN / 2 : BN);
+  for (int kb = 0; kb < p.KB; ++kb) {
+    if (!wait_bounded(r.empty_bar(st.stage), st.phase ^ 1u, r.abort_f, p.status)) return false;
+    const uint32_t sa = r.base + st.stage * STAGE_BYTES, sb = sa + A_BYTES;
+    mbar_expect_tx(r.full_bar(st.stage), STAGE_BYTES);
+    ++st.armed;
+    if (GATEUP) {  // B first: it never waits for another tile
+      tma_load_2d(sb, mapB0, r.full_bar(st.stage), kb * BK, b_row, pb);
+      tma_load_2d(sb + B_BYTES / 2, mapB1, r.full_bar(st.stage), kb * BK, b_row, pb);
+    } else {
+      tma_load_2d(sb, mapB0, r.full_bar(st.stage), kb * BK, b_row, pb);
+    }
+    if (kb == 0 && p.ready_wait &&
+        !wait_count(p.ready_wait + pref[e] + m, p.ready_target, r.abort_f, p.status))
+      return false;
+    tma_load_2d(sa, mapA, r.full_bar(st.stage), kb * BK, a_row, pa);
+    if (++st.stage == STAGES) {
+      st.stage = 0;
+      st.phase ^= 1u;
+    }
+  }
+  return true;
+}
+
+// Tiles blockIdx.x, blockIdx.x + gridDim.x, ... of the tile list.
 template <bool GATEUP, bool FUSED>
 __device__ __forceinline__ bool producer(const CUtensorMap* mapA, const CUtensorMap* mapB0,
                                          const CUtensorMap* mapB1, const TcParams& p,
                                          const int* pref, const Ring& r, ProducerState& st) {
   const int total = pref[p.E] * p.NT;
-  // The resident operand is marked evict_last.  The other one is NOT marked evict_first:
-  // each of its tiles is still read by every CTA of the same m-row / n-column, shortly apart.
-  const uint64_t keep = policy_evict_last(), other = policy_evict_normal();
-  for (int t = blockIdx.x; t < total; t += gridDim.x) {
-    int e, m, n;
-    const bool a_res = decode_tile(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
-    const uint64_t pa = a_res ? keep : other, pb = a_res ? other : keep;
-    const int a_row = off_at<FUSED>(p.offsets, e) + m * BM;
-    const int b_row = e * p.b_rows + n * (GATEUP ? BN / 2 : BN);
-    for (int kb = 0; kb < p.KB; ++kb) {
-      if (!wait_bounded(r.empty_bar(st.stage), st.phase ^ 1u, r.abort_f, p.status)) return false;
-      const uint32_t sa = r.base + st.stage * STAGE_BYTES, sb = sa + A_BYTES;
-      mbar_expect_tx(r.full_bar(st.stage), STAGE_BYTES);
-      tma_load_2d(sa, mapA, r.full_bar(st.stage), kb * BK, a_row, pa);
-      if (GATEUP) {
-        tma_load_2d(sb, mapB0, r.full_bar(st.stage), kb * BK, b_row, pb);
-        tma_load_2d(sb + B_BYTES / 2, mapB1, r.full_bar(st.stage), kb * BK, b_row, pb);
-      } else {
-        tma_load_2d(sb, mapB0, r.full_bar(st.stage), kb * BK, b_row, pb);
-      }
-      ++st.armed;
-      if (++st.stage == STAGES) {
-        st.stage = 0;
-        st.phase ^= 1u;
-      }
-    }
-  }
+  for (int t = blockIdx.x; t < total; t += gridDim.x)
+    if (!producer_tile<GATEUP, FUSED>(mapA, mapB0, mapB1, p, pref, r, st, t)) return false;
   return true;
 }
 
@@ -191,33 +240,39 @@ __device__ __forceinline__ void producer_drain(const Ring& r, ProducerState& st)
 }
 
 // ---------------------------------------------------------------- MMA issuer (one thread)
+// One tile: all K slices into the next TMEM accumulator.
+template <bool BF16>
+__device__ __forceinline__ bool mma_tile(const TcParams& p, const Ring& r, MmaState& st) {
+  constexpr uint32_t idesc = make_idesc(BF16, BM, BN);
+  if (!wait_bounded(r.tempty_bar(st.acc), st.acc_phase ^ 1u, r.abort_f, p.status)) return false;
+  tc_fence_after();
+  const uint32_t d_tmem = r.tmem_base + (uint32_t)(st.acc * BN);
+  for (int kb = 0; kb < p.KB; ++kb) {
+    if (!wait_bounded(r.full_bar(st.stage), st.phase, r.abort_f, p.status)) return false;
+    tc_fence_after();
+    const uint32_t sa = r.base + st.stage * STAGE_BYTES, sb = sa + A_BYTES;
+    const uint64_t da = make_sdesc(sa), db = make_sdesc(sb);
+#pragma unroll
+    for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 elements = 32 bytes along K
+      umma_f16(d_tmem, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
+    umma_commit(r.empty_bar(st.stage));
+    if (++st.stage == STAGES) {
+      st.stage = 0;
+      st.phase ^= 1u;
+    }
+  }
+  umma_commit(r.tfull_bar(st.acc));
+  st.acc ^= 1;
+  if (st.acc == 0) st.acc_phase ^= 1u;
+  return true;
+}
+
 template <bool BF16>
 __device__ __forceinline__ bool mma(const TcParams& p, const int* pref, const Ring& r,
                                     MmaState& st) {
-  constexpr uint32_t idesc = make_idesc(BF16, BM, BN);
   const int total = pref[p.E] * p.NT;
-  for (int t = blockIdx.x; t < total; t += gridDim.x) {
-    if (!wait_bounded(r.tempty_bar(st.acc), st.acc_phase ^ 1u, r.abort_f, p.status)) return false;
-    tc_fence_after();
-    const uint32_t d_tmem = r.tmem_base + (uint32_t)(st.acc * BN);
-    for (int kb = 0; kb < p.KB; ++kb) {
-      if (!wait_bounded(r.full_bar(st.stage), st.phase, r.abort_f, p.status)) return false;
-      tc_fence_after();
-      const uint32_t sa = r.base + st.stage * STAGE_BYTES, sb = sa + A_BYTES;
-      const uint64_t da = make_sdesc(sa), db = make_sdesc(sb);
-#pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 elements = 32 bytes along K
-        umma_f16(d_tmem, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
-      umma_commit(r.empty_bar(st.stage));
-      if (++st.stage == STAGES) {
-        st.stage = 0;
-        st.phase ^= 1u;
-      }
-    }
-    umma_commit(r.tfull_bar(st.acc));
-    st.acc ^= 1;
-    if (st.acc == 0) st.acc_phase ^= 1u;
-  }
+  for (int t = blockIdx.x; t < total; t += gridDim.x)
+    if (!mma_tile<BF16>(p, r, st)) return false;
   return true;
 }
 
@@ -228,12 +283,12 @@ __device__ __forceinline__ void mma_drain(const Ring& r) {
 }
 
 // ---------------------------------------------------------------- epilogue (warps 2..5)
+// One tile: this warp's 32 rows of the accumulator.
 template <bool GATEUP, bool BF16, bool FUSED>
-__device__ __forceinline__ bool epilogue(const TcParams& p, const int* pref, const Ring& r,
-                                         EpilogueState& st, int warp, int lane) {
+__device__ __forceinline__ bool epilogue_tile(const TcParams& p, const int* pref, const Ring& r,
+                                              EpilogueState& st, int t, int warp, int lane) {
   const int q = warp & 3;  // TMEM lane quarter this warp may access
-  const int total = pref[p.E] * p.NT;
-  for (int t = blockIdx.x; t < total; t += gridDim.x) {
+  {
     int e, m, n;
     decode_tile(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
     const bool ok = wait_bounded(r.tfull_bar(st.acc), st.acc_phase, r.abort_f, p.status);
@@ -295,11 +350,27 @@ __device__ __forceinline__ bool epilogue(const TcParams& p, const int* pref, con
       }
     }
     tc_fence_before();
+    if (p.ready_signal) fence_proxy_async_global();  // this lane's rows are read by TMA later
     __syncwarp();
-    if (lane == 0) mbar_arrive(r.tempty_bar(st.acc));
+    if (lane == 0) {
+      mbar_arrive(r.tempty_bar(st.acc));
+      if (p.ready_signal) {
+        __threadfence();
+        atomicAdd(p.ready_signal + pref[e] + m, 1u);
+      }
+    }
     st.acc ^= 1;
     if (st.acc == 0) st.acc_phase ^= 1u;
   }
+  return true;
+}
+
+template <bool GATEUP, bool BF16, bool FUSED>
+__device__ __forceinline__ bool epilogue(const TcParams& p, const int* pref, const Ring& r,
+                                         EpilogueState& st, int warp, int lane) {
+  const int total = pref[p.E] * p.NT;
+  for (int t = blockIdx.x; t < total; t += gridDim.x)
+    if (!epilogue_tile<GATEUP, BF16, FUSED>(p, pref, r, st, t, warp, lane)) return false;
   return true;
 }
 

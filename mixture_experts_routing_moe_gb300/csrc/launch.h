@@ -93,7 +93,9 @@ struct FusedDecodeArgs {
   void* a;
   void* out;
   unsigned* status;
-  unsigned* grid_count;
+  unsigned* grid_count;   // zero at launch
+  unsigned* tile_count;   // zeroed by the kernel
+  unsigned* mtile_ready;  // ceil(T k / 128) + E + 1 counters, zeroed by the kernel
 };
 bool fused_decode_supported(int64_t T, int E, int64_t H, int64_t I, int k, int ldt, int wdt);
 cudaError_t launch_decode_fused(const FusedDecodeArgs& f, int ldt, int wdt, cudaStream_t s);

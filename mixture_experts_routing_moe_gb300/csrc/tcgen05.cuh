@@ -105,6 +105,18 @@ static __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, u
                "r"(d)
                : "memory");
 }
+// Prefetch one box of a tensor map into L2 (no shared memory, no completion to wait for).
+static __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+// Prefetch `bytes` (a multiple of 16) of contiguous global memory at a 16-byte aligned address
+// into L2.
+static __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 // L2 eviction policies: the resident operand is kept (evict_last), the streamed one is not.
 static __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
