@@ -203,9 +203,10 @@ def stage_work(wl: W.Workload, n_active: int):
 
 
 def kernel_source_sha256():
-    """SHA-256 over the sources the forward GEMM kernels compile from (kernel + PTX wrappers)."""
+    """SHA-256 over the sources the forward GEMM kernels compile from (kernels, tile raster,
+    PTX wrappers, helpers)."""
     h = hashlib.sha256()
-    for f in ("experts_tc.cu", "tcgen05.cuh"):
+    for f in ("experts_tc.cu", "gemm_cta.cuh", "tcgen05.cuh", "tiles.cuh", "common.cuh"):
         h.update(open(os.path.join(ROOT, "mixture_experts_routing_moe_gb300", "csrc", f), "rb").read())
     return h.hexdigest()
 

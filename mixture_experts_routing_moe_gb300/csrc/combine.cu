@@ -23,8 +23,8 @@ __global__ void __launch_bounds__(kCombWarps * 32)
   const int64_t gw = (int64_t)blockIdx.x * kCombWarps + (threadIdx.x >> 5);
   const int64_t t = gw / warps_per_token;
   if (t >= T) return;
-  combine_warp<TY, TW, VEC, false>(y, row_of_slot, w, t, H, k, gw - t * warps_per_token, out,
-                                   lane);
+  combine_warp<TY, TW, VEC, false, 1>(y, row_of_slot, w, t, H, k, gw - t * warps_per_token, out,
+                                      lane);
 }
 
 template <typename TY, typename TW>

@@ -9,7 +9,9 @@
 
 namespace moe {
 
-template <typename TY, typename TW, bool VEC, bool COHERENT>
+// BATCH: slots whose loads are issued before their FMAs (8 where few warps are in flight, as in
+// the fused kernel; 1 where many warps already hide the load latency).
+template <typename TY, typename TW, bool VEC, bool COHERENT, int BATCH>
 __device__ __forceinline__ void combine_warp(const TY* __restrict__ y,
                                              const uint32_t* __restrict__ row_of_slot,
                                              const TW* __restrict__ w, int64_t t, int64_t H, int k,
@@ -31,7 +33,7 @@ __device__ __forceinline__ void combine_warp(const TY* __restrict__ y,
     const int nj = min(32, k - jb);
     // groups of kBatch slots: all loads of a group are issued before its FMAs, which still run
     // in slot order
-    constexpr int kBatch = 8;
+    constexpr int kBatch = BATCH;
     for (int j0 = 0; j0 < nj; j0 += kBatch) {
       uint32_t r[kBatch];
       float wj[kBatch];

@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < (int64_t)p.T * wpt;
          it += (int64_t)gridDim.x * kWarps) {
       const int64_t t = (uint32_t)it / (uint32_t)wpt;  // 32-bit division (it < T * wpt)
-      combine_warp<TX, TL, true, true>(reinterpret_cast<const TX*>(p.x_d), p.row_of_slot,
+      combine_warp<TX, TL, true, true, 8>(reinterpret_cast<const TX*>(p.x_d), p.row_of_slot,
                                        reinterpret_cast<const TL*>(p.w), t, p.H, p.k,
                                        it - t * wpt, reinterpret_cast<TX*>(p.out), lane);
     }
