@@ -27,10 +27,38 @@ __device__ __forceinline__ void combine_warp(const TY* __restrict__ y,
     uint32_t my_row = kInvalidRow;
     float my_w = 0.f;
     if (jb + lane < k) {
-      my_row = ld_elem<COHERENT>(row_of_slot + t * k + jb + lane);
-      my_w = Dt<TW>::to_f(ld_elem<COHERENT>(w + t * k + jb + lane));
+      if constexpr (COHERENT) {
+        my_row = ld_elem<true>(row_of_slot + t * k + jb + lane);
+        my_w = Dt<TW>::to_f(ld_elem<true>(w + t * k + jb + lane));
+      } else {
+        my_row = row_of_slot[t * k + jb + lane];
+        my_w = Dt<TW>::to_f(w[t * k + jb + lane]);
+      }
     }
     const int nj = min(32, k - jb);
+    if constexpr (BATCH == 1) {  // one slot at a time: load, then FMA
+      for (int jj = 0; jj < nj; ++jj) {
+        const uint32_t r = __shfl_sync(0xFFFFFFFFu, my_row, jj);
+        const float wj = __shfl_sync(0xFFFFFFFFu, my_w, jj);
+        if (r == kInvalidRow) {
+          poisoned = true;
+          continue;
+        }
+        if (c < chunks) {
+          if (VEC) {
+            Vec16<TY> q;
+            q.u = ld_v4<COHERENT>(y + (int64_t)r * H + c * VW);
+            float f[VW];
+            q.to_float(f);
+#pragma unroll
+            for (int i = 0; i < VW; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+          } else {
+            acc[0] = fmaf(wj, Dt<TY>::to_f(ld_elem<COHERENT>(y + (int64_t)r * H + c)), acc[0]);
+          }
+        }
+      }
+      continue;
+    }
     // groups of kBatch slots: all loads of a group are issued before its FMAs, which still run
     // in slot order
     constexpr int kBatch = BATCH;
