@@ -32,23 +32,29 @@ namespace moe {
 namespace {
 using namespace tc;
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2, B_BYTES = BN * BK * 2, STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int BOX_BYTES = 64 * 128;  // one 64-row x 64-column box
-constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxExperts = 1024;
 constexpr int kChunkBytes = 32 * 32 * 4;             // one 32-row x 32-column FP32 store box
-constexpr int kStagingBytes = 4 * 2 * kChunkBytes;   // two store buffers per epilogue warp
+// Epilogue warps (a multiple of 4: each TMEM lane quarter is read by n/4 warps that split the
+// columns) and ring stages per mode.  Eight WG epilogue warps with a 3-stage ring measured slower
+// on GB300 than four warps with four stages, so every mode uses four and four.
+template <int MODE> constexpr int n_epi_warps() { return 4; }
+template <int MODE> constexpr int n_stages() { return 4; }
+template <int MODE> constexpr int n_threads() { return 64 + 32 * n_epi_warps<MODE>(); }
+template <int MODE> constexpr int staging_bytes() { return MODE == 3 ? n_epi_warps<MODE>() * 2 * kChunkBytes : 0; }
 
 enum Mode { DA = 0, GU = 1, DIN = 2, WG = 3 };
 
 // WG: stages | store buffers | barriers.  Others: stages | barriers | m-tile prefix.
 template <int MODE>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)STAGES * STAGE_BYTES + (MODE == WG ? kStagingBytes : 0) + 256 +
+  return 1024 + (size_t)n_stages<MODE>() * STAGE_BYTES + staging_bytes<MODE>() + 256 +
          (MODE == WG ? 0 : (kMaxExperts + 4) * sizeof(int));
 }
+static_assert(WG == 3, "n_epi_warps / n_stages key on the WG mode number");
 static_assert(smem_bytes<WG>() <= 232448 && smem_bytes<DA>() <= 232448, "shared memory");
 
 // MN-major 128-byte-swizzled operand: 64-column boxes BOX_BYTES apart, 8-row groups 1 KB apart.
@@ -69,6 +75,7 @@ struct BwdParams {
   int MP;           // WG: m-tile pairs per expert
   int M, N;         // WG: output matrix of each expert is M x N
   int a_col0;       // WG: first column of A inside its source matrix (du starts at I)
+  const int* order; // WG: experts by descending row count (ties: lower id first)
   const float* da;  // GU: da [rows, I] FP32
   void* out0;       // DA: da FP32; GU: dgdu; DIN: dinput; WG: C [E, M, N] FP32
   void* out1;       // GU: a
@@ -85,10 +92,11 @@ template <int MODE>
 __device__ __forceinline__ void decode(int t, const int* pref, const BwdParams& p, uint32_t rank,
                                        int& e, int& r0, int& r1, int& m, int& n, bool& share_a) {
   share_a = false;
-  if (MODE == WG) {
+  if (MODE == WG) {  // t: position in the tile list of the experts sorted by rows
     const int per = p.MP * p.NT;
-    e = t / per;
-    const int r = t - e * per;
+    const int sidx = t / per;
+    e = __ldg(p.order + sidx);
+    const int r = t - sidx * per;
     const int mp = r / p.NT;
     n = r - mp * p.NT;
     m = 2 * mp + (int)rank;
@@ -112,6 +120,67 @@ __device__ __forceinline__ void decode(int t, const int* pref, const BwdParams& 
   }
 }
 
+// The j-th tile of pair `pair` (of P), or -1 when the pair has no more.  Other modes: tiles
+// pair, pair + P, ... of the list.  WG: the list holds the experts' tiles in descending order of
+// their rows, so its head is compute-bound (long contractions) and its tail store-bound (the FP32
+// gradient of a short one, or zeros); each pair alternates between the two ends (pair q of the
+// head, then pair q of the tail, ...), even pairs starting at the head and odd pairs at the tail,
+// so at any time about half the pairs keep the tensor pipe busy while the others write.
+template <int MODE>
+__device__ __forceinline__ int tile_at(int j, int pair, int P, int N) {
+  if (MODE != WG) {
+    const long long t = pair + (long long)j * P;
+    return t < N ? (int)t : -1;
+  }
+  const int Hh = (N + 1) / 2, Lh = N / 2;  // head positions [0, Hh), tail positions [Hh, N)
+  const int nf = pair < Hh ? (Hh - pair + P - 1) / P : 0;
+  const int nb = pair < Lh ? (Lh - pair + P - 1) / P : 0;
+  const int both = min(nf, nb);
+  bool head;
+  int i;
+  if (j < 2 * both) {
+    head = ((j & 1) == 0) == ((pair & 1) == 0);
+    i = j >> 1;
+  } else {
+    i = both + (j - 2 * both);
+    head = nf > nb;
+    if (i >= (head ? nf : nb)) return -1;
+  }
+  const int q = pair + i * P;
+  return head ? q : N - 1 - q;
+}
+
+// Experts by descending row count, ties to the lower id (one block, E <= 1024): the order the WG
+// tile list follows.
+__global__ void __launch_bounds__(1024) moe_expert_order(const int32_t* __restrict__ offsets, int E,
+                                                         int* __restrict__ order) {
+  __shared__ unsigned long long key[1024];
+  int n = 1;
+  while (n < E) n <<= 1;
+  for (int i = threadIdx.x; i < n; i += blockDim.x)
+    key[i] = i < E ? ((unsigned long long)(uint32_t)(offsets[i + 1] - offsets[i]) << 32) |
+                         (0xFFFFFFFFu - (uint32_t)i)
+                   : 0ull;
+  __syncthreads();
+  for (int k = 2; k <= n; k <<= 1) {  // bitonic sort, descending
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int ixj = i ^ jj;
+        if (ixj > i) {
+          const unsigned long long a = key[i], b = key[ixj];
+          if (((i & k) == 0) ? (a < b) : (a > b)) {
+            key[i] = b;
+            key[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    order[i] = (int)(0xFFFFFFFFu - (uint32_t)(key[i] & 0xFFFFFFFFull));
+}
+
 // Pair tiles of an expert with n rows (modes other than WG).
 struct PairTiles {
   int NT;
@@ -122,27 +191,27 @@ struct PairTiles {
 };
 
 template <int MODE, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(n_threads<MODE>(), 1)
     moe_experts_bwd_tc(const __grid_constant__ CUtensorMap mapA,
                        const __grid_constant__ CUtensorMap mapB0,
                        const __grid_constant__ CUtensorMap mapB1,
                        const __grid_constant__ CUtensorMap mapX, const BwdParams p) {
   using T = typename std::conditional<BF16, __nv_bfloat16, __half>::type;
+  constexpr int NST = n_stages<MODE>();
   constexpr bool A_MN = MODE == WG, B_MN = MODE != GU;
   extern __shared__ uint8_t tcb_smem_raw[];
   const uint32_t raw = smem_u32(tcb_smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = tcb_smem_raw + (base - raw);
-  const uint32_t staging = base + STAGES * STAGE_BYTES;  // WG store buffers (1 KB aligned)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + STAGES * STAGE_BYTES +
-                                               (MODE == WG ? kStagingBytes : 0));
+  const uint32_t staging = base + NST * STAGE_BYTES;  // WG store buffers (1 KB aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + NST * STAGE_BYTES + staging_bytes<MODE>());
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  auto empty_bar = [&](int s) { return bar0 + 8u * (NST + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * NST + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * NST + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * NST + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * NST + 5);
   volatile int* abort_f = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* pref = reinterpret_cast<int*>(tmem_slot + 4);
 
@@ -150,13 +219,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_rank();
   const int pair = (int)cluster_id_x(), npairs = (int)ncluster_x();
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 2);  // the MMA commits of both CTAs
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
+      mbar_init(tempty_bar(a), n_epi_warps<MODE>());
     }
     mbar_init(drain_bar, 1);
     *abort_f = 0;
@@ -183,7 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool stop = false;
       const uint64_t pol = policy_evict_normal();
-      for (int t = pair; t < total && !stop; t += npairs) {
+      for (int j = 0; !stop; ++j) {
+        const int t = tile_at<MODE>(j, pair, npairs, total);
+        if (t < 0) break;
         int e, r0, r1, m, n;
         bool share_a;
         decode<MODE>(t, pref, p, rank, e, r0, r1, m, n, share_a);
@@ -241,16 +312,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           ++armed;
-          if (++stage == STAGES) {
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
       if (*abort_f) {
-        for (int i = 0; i < min(armed, STAGES); ++i) {
+        for (int i = 0; i < min(armed, NST); ++i) {
           if (stage == 0) {
-            stage = STAGES - 1;
+            stage = NST - 1;
             phase ^= 1u;
           } else {
             --stage;
@@ -265,7 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0, acc = 0;
     uint32_t phase = 0, acc_phase = 0;
     bool stop = false;
-    for (int t = pair; t < total && !stop; t += npairs) {
+    for (int j = 0; !stop; ++j) {
+      const int t = tile_at<MODE>(j, pair, npairs, total);
+      if (t < 0) break;
       int e, r0, r1, m, n;
       bool share_a;
       decode<MODE>(t, pref, p, rank, e, r0, r1, m, n, share_a);
@@ -307,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit_mc(empty_bar(stage), 0x3);  // frees the stage in both CTAs
         }
         __syncwarp();
-        if (++stage == STAGES) {
+        if (++stage == NST) {
           stage = 0;
           phase ^= 1u;
         }
@@ -324,10 +397,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue (warps 2..5)
-    const int q = warp & 3;
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
     int acc = 0, slot = 0;
     uint32_t acc_phase = 0;
-    for (int t = pair; t < total; t += npairs) {
+    for (int j = 0;; ++j) {
+      const int t = tile_at<MODE>(j, pair, npairs, total);
+      if (t < 0) break;
       int e, r0, r1, m, n;
       bool share_a;
       decode<MODE>(t, pref, p, rank, e, r0, r1, m, n, share_a);
@@ -341,13 +416,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool empty = r1 == r0;  // no rows: the gradient is zero
         if (row0 < p.M) {
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
+          // warps 2-5 take column chunks 0-3, warps 6-9 chunks 4-7 (WG has eight epilogue warps)
+          constexpr int kCpw = 8 / (n_epi_warps<MODE>() / 4);
+          const int c0 = ((warp - 2) >> 2) * kCpw;
+          for (int c = c0; c < c0 + kCpw; ++c) {
             const int col0 = n * BN + c * 32;
             if (col0 >= p.N) break;
             uint32_t r[32];
             tmem_ld32(taddr + c * 32, r);
             tmem_wait_ld();
-            const uint32_t buf = staging + (uint32_t)((q * 2 + slot) * kChunkBytes);
+            const uint32_t buf = staging + (uint32_t)(((warp - 2) * 2 + slot) * kChunkBytes);
             if (lane == 0) bulk_wait_read<1>();  // the store that last read `buf` is done with it
             __syncwarp();
 #pragma unroll
@@ -482,7 +560,7 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUten
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(n_threads<MODE>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -515,6 +593,7 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
   float* da = (float*)scratch;
   uint8_t* dgdu = (uint8_t*)scratch + align_up((size_t)rows * I * 4, 256);
   uint8_t* abuf = dgdu + align_up((size_t)rows * 2 * I * 2, 256);
+  int* order = (int*)(abuf + align_up((size_t)rows * I * 2, 256));  // [E] for the WG tile order
   const int64_t mt_upper = (rows + BM - 1) / BM + E;  // >= m-tiles; pair tiles <= mt * ceil(NT/2)
   CUtensorMap mAh;  // A with 64-row boxes: the halves of a shared A tile
   CUtensorMap mA, mB0, mB1;
@@ -562,7 +641,11 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
   err = launch_mode<DIN, BF16>(mA, mB0, mB1, mAh, p, mt_upper * ((p.NT + 1) / 2), dev, s);
   if (err != cudaSuccess) return err;
 
-  // 4. weight gradients, contracted over each expert's rows
+  // 4. weight gradients, contracted over each expert's rows, experts ordered by row count
+  moe_expert_order<<<1, 1024, 0, s>>>(offsets, E, order);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  p.order = order;
   CUtensorMap mX, mC;
   if (!make_map_2d(&mA, dgdu, BF16, 2 * (int64_t)I, rows, 64, 64) ||
       !make_map_2d(&mX, x_d, BF16, H, rows, 64, 64) ||
@@ -599,7 +682,7 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
 
 size_t experts_backward_tc_scratch_bytes(int64_t rows, int64_t I) {
   return align_up((size_t)rows * I * 4, 256) + align_up((size_t)rows * 2 * I * 2, 256) +
-         align_up((size_t)rows * I * 2, 256);
+         align_up((size_t)rows * I * 2, 256) + 1024 * sizeof(int);
 }
 
 cudaError_t launch_experts_backward_tc(const void* x_d, const int32_t* offsets, int64_t rows,
