@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(256)
   if (row >= T_) return;
   const uint4* src = logits + row * NV;
   uint32_t top[8];
-  uint32_t minv = 0xFFFFFFFFu;  // smallest monotone value (catches negative NaNs)
+  uint32_t rawmax = 0u;  // per-half unsigned max of the raw bits: above -inf only for a negative NaN
   float m = -INFINITY, s = 0.f;
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
@@ -107,9 +107,12 @@ __global__ void __launch_bounds__(256)
     uint32_t g[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      // monotone map of both 16-bit halves: negative -> all bits flipped, else sign bit set
-      const uint32_t t = w[i] ^ ((((w[i] >> 15) & 0x00010001u) * 0xFFFFu) | 0x80008000u);
-      minv = min(minv, min(t & 0xFFFFu, t >> 16));
+      // monotone map of both 16-bit halves: negative -> all bits flipped, else sign bit set.
+      // prmt with selector 0xBB99 replicates each half's sign bit over the half (0xFFFF / 0).
+      uint32_t sm;
+      asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(sm) : "r"(w[i]));
+      const uint32_t t = w[i] ^ (sm | 0x80008000u);
+      rawmax = __vmaxu2(rawmax, w[i]);
       const uint32_t e0 = v * 8 + i * 2;
       g[2 * i] = (t << 16) | (0xFFFFu - e0);
       g[2 * i + 1] = (t & 0xFFFF0000u) | (0xFFFFu - (e0 + 1));
@@ -140,11 +143,11 @@ __global__ void __launch_bounds__(256)
     }
   }
   // poisoned: largest value NaN / +inf / -inf (the last means every value is -inf), or a
-  // negative NaN at the bottom
+  // negative NaN anywhere (its raw bits exceed those of -inf)
   const uint32_t tb = top[0] >> 16;
   const uint32_t vb0 = (tb & 0x8000u) ? (tb & 0x7FFFu) : (~tb & 0xFFFFu);
-  const uint32_t vbm = (minv & 0x8000u) ? (minv & 0x7FFFu) : (~minv & 0xFFFFu);
-  const bool poisoned = (vb0 & 0x7FFFu) >= EXPMASK || ((vbm & 0x7FFFu) > EXPMASK);
+  const uint32_t rmax = max(rawmax & 0xFFFFu, rawmax >> 16);  // negative NaN: above 0x8000|EXPMASK
+  const bool poisoned = (vb0 & 0x7FFFu) >= EXPMASK || rmax > (0x8000u | EXPMASK);
   const float x0 = bits16_to_float<T>(vb0);
   float ex[8], sel = 0.f;
 #pragma unroll

@@ -30,7 +30,13 @@ def _logits(T, E, dt, seed, std=2.0, ties=True, poison=True):
         l[5, :] = float("-inf")
         if E > 2:
             l[7, : E - 2] = float("-inf")           # finite row with few finite entries
-    return l.to(dt)
+    l = l.to(dt)
+    if poison and T >= 10:
+        # a NaN with the sign bit set (bit pattern), which sorts below -inf as raw bits
+        bits = {torch.float32: (torch.int32, -4194303), torch.float16: (torch.int16, -511),
+                torch.bfloat16: (torch.int16, -63)}[dt]
+        l.view(bits[0])[9, E // 3] = bits[1]
+    return l
 
 
 # ------------------------------------------------------------------------------------ route
