@@ -44,7 +44,10 @@ constexpr int kChunkBytes = 32 * 32 * 4;             // one 32-row x 32-column F
 template <int MODE> constexpr int n_epi_warps() { return 4; }
 template <int MODE> constexpr int n_stages() { return 4; }
 template <int MODE> constexpr int n_threads() { return 64 + 32 * n_epi_warps<MODE>(); }
-template <int MODE> constexpr int staging_bytes() { return MODE == 3 ? n_epi_warps<MODE>() * 2 * kChunkBytes : 0; }
+// WG store buffers per epilogue warp.  Four (with a 3-stage ring to make room) measured slower
+// than two with four stages.
+constexpr int kStoreBufs = 2;
+template <int MODE> constexpr int staging_bytes() { return MODE == 3 ? n_epi_warps<MODE>() * kStoreBufs * kChunkBytes : 0; }
 
 enum Mode { DA = 0, GU = 1, DIN = 2, WG = 3 };
 
@@ -425,8 +428,9 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
             uint32_t r[32];
             tmem_ld32(taddr + c * 32, r);
             tmem_wait_ld();
-            const uint32_t buf = staging + (uint32_t)(((warp - 2) * 2 + slot) * kChunkBytes);
-            if (lane == 0) bulk_wait_read<1>();  // the store that last read `buf` is done with it
+            const uint32_t buf =
+                staging + (uint32_t)(((warp - 2) * kStoreBufs + slot) * kChunkBytes);
+            if (lane == 0) bulk_wait_read<kStoreBufs - 1>();  // the store that last read `buf` is done
             __syncwarp();
 #pragma unroll
             for (int j = 0; j < 8; ++j) {  // 16-byte chunk j of this lane's row, 128-byte swizzle
@@ -442,7 +446,7 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
               tma_store_3d(&mapX, buf, col0, row0, e);
               bulk_commit();
             }
-            slot ^= 1;
+            slot = slot + 1 == kStoreBufs ? 0 : slot + 1;
           }
         }
       } else {

@@ -65,6 +65,12 @@ WORKLOADS = {
     # enough (2.8 GB of weights) for multi-pass counter captures
     "skewed_e32": Workload("skewed_e32", T=2048, H=7168, I=2048, E=32, top_k=8,
                            renormalize=True, dtype="bf16", seed=6, zipf_s=1.2),
+    # profiling cases of the expert backward (about 1.3 GB on the device): every expert with
+    # exactly 512 rows (top_k = E), and 16 experts under a steep Zipf bias
+    "wgrad_uniform": Workload("wgrad_uniform", T=512, H=4096, I=2048, E=8, top_k=8,
+                              renormalize=True, dtype="bf16", seed=7),
+    "wgrad_skewed": Workload("wgrad_skewed", T=1024, H=4096, I=2048, E=16, top_k=4,
+                             renormalize=True, dtype="bf16", seed=8, zipf_s=1.5),
 }
 
 
