@@ -66,6 +66,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward chain (combine, experts, dispatch, router) instead")
+    ap.add_argument("--router", choices=["softmax", "sigmoid"], default="softmax",
+                    help="sigmoid: time group-limited sigmoid routing (8 groups, top 4, top-two "
+                         "group scores) alone and in the whole layer")
     return ap.parse_args()
 
 
@@ -438,6 +441,80 @@ def run_backward(args):
     print(json.dumps(line), flush=True)
 
 
+def run_sigmoid(args):
+    """Group-limited sigmoid routing (8 groups, best 4 by the sum of their two largest corrected
+    scores, top_k of the workload, a per-expert FP32 correction bias): the router alone against
+    HBM, and the whole layer (moe_forward_sigmoid_grouped) in tokens/s."""
+    import mixture_experts_routing_moe_gb300 as moe
+    from mixture_experts_routing_moe_gb300 import build as build_mod
+    build_mod.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]
+    G, SG = 8, 4
+    inp = W.make_layer_inputs(wl, dev)
+    x, logits, gate, up, down = (inp[k] for k in ("x", "logits", "gate", "up", "down"))
+    bias = (0.01 * torch.randn(wl.E, generator=torch.Generator(device=dev).manual_seed(9),
+                               device=dev)).float()
+    out = torch.empty_like(x)
+    ws = torch.empty(moe.forward_workspace_bytes(wl.T, wl.E, wl.H, wl.I, wl.top_k, logits.dtype,
+                                                 x.dtype), dtype=torch.uint8, device=dev)
+    idx = torch.empty(wl.T, wl.top_k, dtype=torch.uint32, device=dev)
+    w = torch.empty(wl.T, wl.top_k, dtype=logits.dtype, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # larger than L2
+
+    def route():
+        moe.moe_route_sigmoid_grouped(logits, wl.top_k, G, SG, True, wl.renormalize, 1.0, bias,
+                                      idx=idx, w=w)
+
+    def layer():
+        moe.moe_forward_sigmoid_grouped(x, logits, gate, up, down, wl.top_k, G, SG, True,
+                                        wl.renormalize, 1.0, bias, out=out, ws=ws)
+
+    def timed(fn, n, flush_l2):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        ms = []
+        for _ in range(n):
+            if flush_l2:
+                flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return float(np.median(ms))
+    sampler = ClockSampler(dev)
+    sampler.start()
+    time.sleep(0.3)
+    route_ms = timed(route, args.steps, True)
+    layer_ms = timed(layer, args.steps, False)
+    clocks = sampler.stop()
+    st = moe.moe_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
+    es = logits.element_size()
+    nbytes = wl.T * wl.E * es + wl.E * 4 + wl.T * wl.top_k * (4 + es)
+    pk, pk_src = peaks()
+    gbs = nbytes / (route_ms / 1e3) / 1e9
+    line = {"metric": "MoE fwd tokens/s with group-limited sigmoid routing; router GB/s vs HBM",
+            "value": wl.T / (layer_ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": layer_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic",
+            "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
+                       "top_k": wl.top_k, "groups": G, "selected_groups": SG,
+                       "group_top_two": True, "l2": "flushed before each router launch"},
+            "roofline": {"kernel": "moe_route_sigmoid_kernel (float64 selection, warp per row)",
+                         "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"], "peak_source": f"{pk_src} HBM copy",
+                         "traffic": None, "algorithmic_bytes_per_launch": nbytes},
+            "stages_ms": {"route_sigmoid": route_ms, "layer": layer_ms},
+            "gpu_launches": args.steps * (1 + 1 + 4 + 2 + 1), "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args):
     import mixture_experts_routing_moe_gb300 as moe
     from mixture_experts_routing_moe_gb300 import build as build_mod
@@ -622,6 +699,8 @@ def main():
         run_route_only(args)
     elif args.backward:
         run_backward(args)
+    elif args.router == "sigmoid":
+        run_sigmoid(args)
     else:
         run_ours(args)
 

@@ -8,10 +8,17 @@
 // chosen experts, divided by their sum when renormalising, times scale, rounded to the logits
 // dtype.  Rows whose corrected scores hold a NaN get NaN weights and ids 0..k-1.
 //
-// The selection (sigmoid, correction, group scores, ranking) is computed in float64 so that it is
-// the same decision as the float64 reference.  One warp owns a row: lane i holds experts
-// i, i + 32, ...; s and c are staged in shared memory for the group scores; the group and expert
-// choices are rounds of warp argmax over (score, -id) pairs.
+// The selection (sigmoid, correction, group scores, ranking) is the decision float64 arithmetic
+// makes, as in the float64 reference.  One warp owns a row: lane i holds experts i, i + 32, ...;
+// the group and expert choices are rounds of warp argmax over (score, -id) pairs.  Each row is
+// first decided in FP32 (accurate expf, IEEE division): with the FP32 error of every corrected
+// score bounded by E_c = 5e-7 + 1.2e-7 max|c| (expf within 2 ulp, the division and the additions
+// rounded once each), the FP32 choice is the float64 choice whenever every margin it rests on --
+// last chosen group vs the best other group, each chosen expert vs the next one, the k-th vs the
+// best unchosen candidate -- exceeds twice the bound on the two scores compared.  Those rows take
+// their k weights from float64 sigmoids of the chosen experts; every other row (a near or exact
+// tie, a NaN or infinite score) is decided again entirely in float64.  Either way the indices
+// and weights are the float64 path's.
 #include "common.cuh"
 #include "launch.h"
 
@@ -33,6 +40,160 @@ __device__ __forceinline__ void warp_argmax(double& v, int& id) {
   }
 }
 
+// float argmax over (v, id) with the same rule; all lanes get the winner
+__device__ __forceinline__ void warp_argmax_f(float& v, int& id) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    const int oi = __shfl_xor_sync(0xFFFFFFFFu, id, o);
+    if (ov > v || (ov == v && oi < id)) {
+      v = ov;
+      id = oi;
+    }
+  }
+}
+
+// The FP32 attempt at one row (see the file comment).  Returns true when it wrote the row's ids
+// and weights; false leaves the row to the float64 path.  sm: per-warp scratch of at least
+// E + 2 G floats.  Every lane of the warp calls it and gets the same answer.
+template <typename T, int C>
+__device__ __forceinline__ bool sigmoid_row_fp32(const T* __restrict__ src,
+                                                 const float* __restrict__ bias, int64_t row, int E,
+                                                 int k, int G, int SG, int top_two, int renorm,
+                                                 float scale, float* sm, int lane,
+                                                 uint32_t* __restrict__ idx_out,
+                                                 T* __restrict__ w_out) {
+  if (k > 32) return false;  // slot r's expert is kept in lane r
+  const int gs = E / G;
+  float c[C];
+  float amax = 0.f;
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const float x = Dt<T>::to_f(src[e]);
+      const float sg = 1.0f / (1.0f + expf(-x));
+      c[i] = sg + (bias ? bias[e] : 0.f);
+      finite &= isfinite(c[i]);
+      amax = fmaxf(amax, fabsf(c[i]));
+      sm[e] = c[i];
+    } else {
+      c[i] = 0.f;
+    }
+  }
+  if (!__all_sync(0xFFFFFFFFu, finite)) return false;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const float ec = 5e-7f + 1.2e-7f * amax;                       // bound on |c32 - c64|
+  const float eg = (top_two ? 2.f * ec : ec) + 2.4e-7f * amax;    // bound on a group score
+  __syncwarp();
+  float* gsc = sm + E;  // [G]
+  for (int g = lane; g < G; g += 32) {
+    float b1 = -INFINITY, b2 = -INFINITY;
+    for (int j = 0; j < gs; ++j) {
+      const float v = sm[g * gs + j];
+      if (v > b1) {
+        b2 = b1;
+        b1 = v;
+      } else if (v > b2) {
+        b2 = v;
+      }
+    }
+    gsc[g] = top_two ? b1 + b2 : b1;
+  }
+  __syncwarp();
+  // SG groups, then (when SG < G) the best other group: its margin to the last chosen one
+  unsigned long long chosen_lo = 0, chosen_hi = 0;
+  float last = 0.f;
+  for (int r = 0; r < SG + (SG < G ? 1 : 0); ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+    for (int g = lane; g < G; g += 32) {
+      const bool taken = g < 64 ? (chosen_lo >> g) & 1ull : (chosen_hi >> (g - 64)) & 1ull;
+      const float v = gsc[g];
+      if (!taken && (bi == 0x7FFFFFFF || v > bv || (v == bv && g < bi))) {
+        bv = v;
+        bi = g;
+      }
+    }
+    warp_argmax_f(bv, bi);
+    if (r == SG) {
+      if (!(last - bv > 2.f * eg)) return false;
+      break;
+    }
+    last = bv;
+    if (bi < 64) chosen_lo |= 1ull << bi;
+    else chosen_hi |= 1ull << (bi - 64);
+  }
+  // top_k experts of the chosen groups, then the best unchosen one; all margins must clear 2 ec
+  const int cand = SG * gs;
+  unsigned avail = 0;  // this lane's elements that are candidates and not taken yet
+#pragma unroll
+  for (int i = 0; i < C; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      const int g = e / gs;
+      if (g < 64 ? (chosen_lo >> g) & 1ull : (chosen_hi >> (g - 64)) & 1ull) avail |= 1u << i;
+    }
+  }
+  float prev = 0.f, my_c = 0.f;
+  int my_id = -1;
+  for (int r = 0; r < k + (k < cand ? 1 : 0); ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7FFFFFFF;
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      const int e = lane + 32 * i;
+      if (((avail >> i) & 1u) && (bi == 0x7FFFFFFF || c[i] > bv || (c[i] == bv && e < bi))) {
+        bv = c[i];
+        bi = e;
+      }
+    }
+    warp_argmax_f(bv, bi);
+    if (r > 0 && !(prev - bv > 2.f * ec)) return false;
+    if (r == k) break;
+    prev = bv;
+    if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
+    if (lane == r) my_id = bi;  // slot r's expert lives in lane r (k <= 32 here)
+  }
+  // Weights.  16-bit outputs: w in FP32 (relative error below kWeightErr); when w (1 - err) and
+  // w (1 + err) round to the same 16-bit value, that value is the rounding of the float64 weight.
+  // Otherwise, and for f32 outputs, the float64 path's arithmetic: sigmoids of the chosen experts
+  // in float64, summed in slot order.
+  float w32 = 0.f;
+  if (lane < k) w32 = 1.0f / (1.0f + expf(-Dt<T>::to_f(src[my_id])));
+  float sel32 = 0.f;
+  for (int j = 0; j < k; ++j) sel32 += __shfl_sync(0xFFFFFFFFu, w32, j);
+  bool exact = sizeof(T) == 2;
+  T wout = Dt<T>::from_f(0.f);
+  if (exact && lane < k) {
+    constexpr float kWeightErr = 4e-6f;  // s: 4e-7 each; the sum of <= 32: 32 x 4e-7; / and *: 1e-7
+    const float w = (renorm ? w32 / sel32 : w32) * scale;
+    wout = Dt<T>::from_f(w);
+    const T lo = Dt<T>::from_f(w * (1.f - kWeightErr)), hi = Dt<T>::from_f(w * (1.f + kWeightErr));
+    exact = Dt<T>::to_f(lo) == Dt<T>::to_f(wout) && Dt<T>::to_f(hi) == Dt<T>::to_f(wout);
+  }
+  if (!__all_sync(0xFFFFFFFFu, exact)) {
+    double sv = 0.0;
+    if (lane < k) {
+      const double x = (double)Dt<T>::to_f(src[my_id]);
+      sv = 1.0 / (1.0 + exp(-x));
+    }
+    double sel = 0.0;
+    for (int j = 0; j < k; ++j) sel += __shfl_sync(0xFFFFFFFFu, sv, j);
+    double w = sv;
+    if (renorm) w = w / sel;
+    w *= (double)scale;
+    wout = Dt<T>::from_f((float)w);
+  }
+  if (lane < k) {
+    idx_out[row * k + lane] = (uint32_t)my_id;
+    w_out[row * k + lane] = wout;
+  }
+  return true;
+}
+
 template <typename T, int C>
 __global__ void __launch_bounds__(kSigWarps * 32)
     moe_route_sigmoid_kernel(const T* __restrict__ logits, const float* __restrict__ bias,
@@ -47,6 +208,9 @@ __global__ void __launch_bounds__(kSigWarps * 32)
   double* gsc = cs + E;
   const int gs = E / G;
   const T* src = logits + row * (int64_t)E;
+  if (sigmoid_row_fp32<T, C>(src, bias, row, E, k, G, SG, top_two, renorm, scale,
+                             reinterpret_cast<float*>(cs), lane, idx_out, w_out))
+    return;
 
   double s[C], c[C];
   bool nan_seen = false;

@@ -50,6 +50,27 @@ def test_sigmoid_route_matches_oracle(dt, E, G, SG, k, top2, renorm, with_bias):
     check_weights(w, rw, f"sigmoid {name} E={E} G={G} k={k}")
 
 
+@pytest.mark.parametrize("top2", [True, False])
+def test_sigmoid_route_near_ties(top2):
+    """f32 logits a few ulps apart around a handful of values: most rows fall inside the FP32
+    error margin of the first pass and are decided in float64, the rest by the FP32 pass; the
+    indices must be the float64 decision either way."""
+    T, E, G, SG, k = 2000, 64, 8, 3, 6
+    g = torch.Generator().manual_seed(11)
+    base = torch.tensor([-1.0, 0.25, 0.5, 1.75], dtype=torch.float32)[
+        torch.randint(0, 4, (T, E), generator=g)]
+    ulps = torch.randint(-4, 5, (T, E), generator=g).to(torch.int32)
+    l = (base.view(torch.int32) + ulps).view(torch.float32)
+    l[: T // 2] += torch.randn(T // 2, E, generator=g) * 3          # half the rows well apart
+    bias = (torch.randn(E, generator=g) * 1e-7).float()              # corrections of a few ulps
+    idx, w = moe.moe_route_sigmoid_grouped(l.to(DEV), k, G, SG, top2, True, 1.0, bias.to(DEV))
+    torch.cuda.synchronize()
+    ridx, rw = O.route_sigmoid_grouped(O.to_f64(*storage(l)), bias.double().numpy(), k, G, SG,
+                                       top2, True, 1.0, "f32")
+    np.testing.assert_array_equal(u32(idx), ridx)
+    check_weights(w, rw, "sigmoid near ties")
+
+
 def test_sigmoid_route_large_batch():
     T, E = 16384, 256
     wl = W.WORKLOADS["skewed"]
