@@ -13,6 +13,7 @@
 // memory, ragged per-expert row groups found from the device-side offsets (rows for the
 // activation GEMMs, the contraction dimension for the weight gradients).  Sums over slots are
 // in slot order and sums inside a tile in a fixed order, so results are run-to-run identical.
+#include "combine_core.cuh"
 #include "common.cuh"
 #include "launch.h"
 #include "tiles.cuh"
@@ -57,6 +58,66 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Vectorised combine backward for top_k <= 8 and 16-byte rows: one warp per token, lanes over
+// 16-byte column chunks; per chunk the k rows of y are loaded together, dexpert = w dout is
+// written (the same values as the scalar kernel) and the k dot products accumulate in a fixed
+// order (chunk by chunk, then a xor tree), so the result is the same on every run.
+template <typename TY, typename TW>
+__global__ void __launch_bounds__(256)
+    moe_combine_bwd_vec(const TY* __restrict__ y, const uint32_t* __restrict__ row_of_slot,
+                        const TW* __restrict__ w, const TY* __restrict__ dout, int64_t T_,
+                        int64_t H, int k, TY* __restrict__ dexpert, float* __restrict__ dweights) {
+  constexpr int VW = 16 / (int)sizeof(TY);
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T_) return;
+  uint32_t r[8];
+  float wj[8], dot[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    r[j] = j < k ? row_of_slot[t * k + j] : kInvalidRow;
+    wj[j] = j < k ? Dt<TW>::to_f(w[t * k + j]) : 0.f;
+    dot[j] = 0.f;
+  }
+  const int64_t chunks = H / VW;
+  for (int64_t c = lane; c < chunks; c += 32) {
+    Vec16<TY> g;
+    g.u = ld_nc_v4(dout + t * H + c * VW);
+    float gf[VW];
+    g.to_float(gf);
+    uint4 yv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (r[j] != kInvalidRow) yv[j] = ld_nc_v4(y + (int64_t)r[j] * H + c * VW);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (r[j] != kInvalidRow) {
+        Vec16<TY> q;
+        q.u = yv[j];
+        float yf[VW], of[VW];
+        q.to_float(yf);
+        float d = 0.f;
+#pragma unroll
+        for (int i = 0; i < VW; ++i) {
+          d = fmaf(gf[i], yf[i], d);
+          of[i] = wj[j] * gf[i];
+        }
+        dot[j] += d;
+        Vec16<TY> o;
+        o.from_float(of);
+        st_v4(dexpert + (int64_t)r[j] * H + c * VW, o.u);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot[j] += __shfl_xor_sync(0xFFFFFFFFu, dot[j], o);
+    if (lane == 0 && j < k)
+      dweights[t * k + j] = r[j] == kInvalidRow ? __int_as_float(0x7FC00000) : dot[j];
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256)
     moe_dispatch_bwd_kernel(const T* __restrict__ dinput, const uint32_t* __restrict__ row_of_slot,
@@ -72,6 +133,18 @@ __global__ void __launch_bounds__(256)
     }
     dx[t * H + h] = Dt<T>::from_f(acc);
   }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+    moe_dispatch_bwd_vec(const T* __restrict__ dinput, const uint32_t* __restrict__ row_of_slot,
+                         int64_t T_, int64_t H, int k, int64_t wpt, T* __restrict__ dx) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t t = gw / wpt;
+  if (t >= T_) return;
+  combine_warp<T, float, true, false, 1>(dinput, row_of_slot, nullptr, t, H, k, gw - t * wpt, dx,
+                                         lane);
 }
 
 // ------------------------------------------------------------------ ragged row GEMMs
@@ -267,8 +340,14 @@ template <typename TY, typename TW>
 cudaError_t combine_bwd_tw(const void* y, const uint32_t* ros, const void* w, const void* dout,
                            int64_t T_, int64_t H, int k, void* dexpert, float* dweights,
                            cudaStream_t s) {
-  moe_combine_bwd_kernel<TY, TW><<<(unsigned)((T_ + 7) / 8), 256, 0, s>>>(
-      (const TY*)y, ros, (const TW*)w, (const TY*)dout, T_, H, k, (TY*)dexpert, dweights);
+  const bool vec = k <= 8 && (H * (int64_t)sizeof(TY)) % 16 == 0 && (uintptr_t)y % 16 == 0 &&
+                   (uintptr_t)dout % 16 == 0 && (uintptr_t)dexpert % 16 == 0;
+  if (vec)
+    moe_combine_bwd_vec<TY, TW><<<(unsigned)((T_ + 7) / 8), 256, 0, s>>>(
+        (const TY*)y, ros, (const TW*)w, (const TY*)dout, T_, H, k, (TY*)dexpert, dweights);
+  else
+    moe_combine_bwd_kernel<TY, TW><<<(unsigned)((T_ + 7) / 8), 256, 0, s>>>(
+        (const TY*)y, ros, (const TW*)w, (const TY*)dout, T_, H, k, (TY*)dexpert, dweights);
   return cudaGetLastError();
 }
 template <typename TY>
@@ -325,6 +404,28 @@ cudaError_t launch_combine_backward(const void* y, int ydt, const uint32_t* ros,
 
 cudaError_t launch_dispatch_backward(const void* dinput, int dt, const uint32_t* ros, int64_t T_,
                                      int64_t H, int k, void* dx, cudaStream_t s) {
+  // 16-byte rows: the combine's warp routine with unit weights (a token spread over
+  // ceil(H / (32 x 16 B)) warps, FP32 slot-order sums, NaN for a slot without a row)
+  const int es = dt == MOE_F32 ? 4 : 2;
+  if ((H * es) % 16 == 0 && (uintptr_t)dinput % 16 == 0 && (uintptr_t)dx % 16 == 0 &&
+      (dt == MOE_F32 || dt == MOE_F16 || dt == MOE_BF16)) {
+    const int64_t chunks = H * es / 16, wpt = (chunks + 31) / 32;
+    const unsigned nb = (unsigned)((T_ * wpt + 7) / 8);
+    switch (dt) {
+      case MOE_F32:
+        moe_dispatch_bwd_vec<float><<<nb, 256, 0, s>>>((const float*)dinput, ros, T_, H, k, wpt,
+                                                        (float*)dx);
+        break;
+      case MOE_F16:
+        moe_dispatch_bwd_vec<__half><<<nb, 256, 0, s>>>((const __half*)dinput, ros, T_, H, k, wpt,
+                                                         (__half*)dx);
+        break;
+      default:
+        moe_dispatch_bwd_vec<__nv_bfloat16><<<nb, 256, 0, s>>>(
+            (const __nv_bfloat16*)dinput, ros, T_, H, k, wpt, (__nv_bfloat16*)dx);
+    }
+    return cudaGetLastError();
+  }
   const unsigned blocks = (unsigned)((T_ + 7) / 8);
   switch (dt) {
     case MOE_F32:

@@ -1,7 +1,8 @@
 // One warp's share of the combine (ruDNN user guide, §3 "MoE-Workflow" / §6 "MoE aufrufen"):
 // columns [32 c0 VW, 32 c0 VW + 32 VW) of out[t] = sum_j w[t, j] * y[row_of_slot[t*k + j]],
 // FP32 accumulation in the fixed slot order j = 0..k-1, one rounding to the output dtype.  A
-// slot without a row (poisoned routing) makes the token's output NaN.  COHERENT reads y, the map
+// slot without a row (poisoned routing) makes the token's output NaN.  With w == nullptr every
+// weight is 1 (fmaf(1, v, acc) rounds as acc + v): the slot sum of dispatch_backward.  COHERENT reads y, the map
 // and the weights through L2 only (they were written earlier in the same launch).
 #pragma once
 
@@ -29,10 +30,10 @@ __device__ __forceinline__ void combine_warp(const TY* __restrict__ y,
     if (jb + lane < k) {
       if constexpr (COHERENT) {
         my_row = ld_elem<true>(row_of_slot + t * k + jb + lane);
-        my_w = Dt<TW>::to_f(ld_elem<true>(w + t * k + jb + lane));
+        my_w = w ? Dt<TW>::to_f(ld_elem<true>(w + t * k + jb + lane)) : 1.f;
       } else {
         my_row = row_of_slot[t * k + jb + lane];
-        my_w = Dt<TW>::to_f(w[t * k + jb + lane]);
+        my_w = w ? Dt<TW>::to_f(w[t * k + jb + lane]) : 1.f;  // no weights: the plain sum
       }
     }
     const int nj = min(32, k - jb);

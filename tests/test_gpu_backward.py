@@ -55,8 +55,10 @@ def test_experts_backward_matches_oracle(dt, counts, H, I):
 
 
 @pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
-def test_combine_and_dispatch_backward_match_oracle(ydt):
-    T, k, H, E = 150, 3, 96, 7
+@pytest.mark.parametrize("T,k,H,E", [(150, 3, 96, 7),     # 16-byte rows, k <= 8: vector kernels
+                                     (60, 12, 40, 16),    # k > 8: scalar combine backward
+                                     (90, 5, 41, 9)])     # 82 / 164-byte rows: scalar kernels
+def test_combine_and_dispatch_backward_match_oracle(ydt, T, k, H, E):
     gen = torch.Generator().manual_seed(5)
     idx = torch.stack([torch.randperm(E, generator=gen)[:k] for _ in range(T)]).numpy().astype(np.uint32)
     _, _, _, ros = O.dispatch(idx, E)
@@ -72,6 +74,32 @@ def test_combine_and_dispatch_backward_match_oracle(ydt):
     dx = moe.moe_dispatch_backward(de, ros_t, T, k)
     rdx = O.dispatch_backward(O.to_f64(*storage(de.cpu())), ros, T, k)
     assert rel_max_err(f64(dx), rdx) <= (1e-6 if ydt == torch.float32 else 2.0 ** -8)
+
+
+@pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("H", [96, 41])
+def test_backward_invalid_slot_gives_nan(ydt, H):
+    """A slot whose row_of_slot is 0xFFFFFFFF (an expert id >= E never dispatched): its dweight is
+    NaN, its token's dx row is NaN, and the dexpert rows of the other slots are still written."""
+    T, k, E = 40, 4, 6
+    gen = torch.Generator().manual_seed(8)
+    idx = torch.stack([torch.randperm(E, generator=gen)[:k] for _ in range(T)]).numpy().astype(np.uint32)
+    _, _, _, ros = O.dispatch(idx, E)
+    ros = ros.copy()
+    ros[3 * k + 1] = 0xFFFFFFFF
+    y = torch.randn(T * k, H, generator=gen).to(ydt)
+    w = torch.rand(T, k, generator=gen).to(ydt)
+    dout = torch.randn(T, H, generator=gen).to(ydt)
+    ros_t = torch.from_numpy(ros.view(np.int32)).to(DEV).view(torch.uint32)
+    de, dw = moe.moe_combine_backward(y.to(DEV), ros_t, w.to(DEV), dout.to(DEV))
+    dx = moe.moe_dispatch_backward(de, ros_t, T, k)
+    torch.cuda.synchronize()
+    dw, dx, de = dw.cpu(), dx.float().cpu(), de.float().cpu()
+    assert torch.isnan(dw[3, 1]) and not torch.isnan(dw[3, [0, 2, 3]]).any()
+    assert torch.isnan(dx[3]).all() and not torch.isnan(dx[torch.arange(T) != 3]).any()
+    r0 = int(ros[3 * k])   # a valid slot of the same token: dexpert = w dout
+    ref = (w[3, 0].float() * dout[3].float()).to(ydt).float()
+    assert torch.equal(de[r0], ref)
 
 
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
