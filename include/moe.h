@@ -212,7 +212,8 @@ int moe_combine(const void* y, int ydt, const uint32_t* row_of_slot, const void*
  * ws: at least moe_forward_workspace_bytes(T, E, H, I, top_k, ldt, wdt) bytes, 256-byte aligned.
  * Short batches (see moe_forward_fused) run as ONE cooperative launch that performs the same
  * steps between grid barriers; longer ones as the staged launches.  Both give the same routing,
- * dispatch order and combine order.
+ * dispatch order and combine order.  If the cooperative launch cannot have all its blocks
+ * resident (another context holds SMs), the staged launches run instead.
  */
 size_t moe_forward_workspace_bytes(int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
                                    int ldt, int wdt);

@@ -185,7 +185,10 @@ int run_forward(const void* x, const void* logits, int ldt, const void* gate, co
     f.grid_count = (unsigned*)(b + 64);
     f.tile_count = (unsigned*)(b + 128);
     f.mtile_ready = (unsigned*)(b + L.ready);
-    return cuda_status(launch_decode_fused(f, ldt, wdt, s));
+    const cudaError_t ferr = launch_decode_fused(f, ldt, wdt, s);
+    if (ferr != cudaErrorCooperativeLaunchTooLarge) return cuda_status(ferr);
+    // not all CTAs could be resident (the GPU is shared): the staged launches below instead
+    (void)cudaGetLastError();
   }
   if (cudaMemsetAsync(status, 0, sizeof(unsigned), s) != cudaSuccess) return MOE_ERR_CUDA;
   if (!record(events, 0, s)) return MOE_ERR_CUDA;
