@@ -31,7 +31,11 @@ struct Cursor {
 struct FwdLayout {
   size_t idx, w, ros, tor, offsets, hist, ready, xd, a, total;
 };
-size_t ready_bytes(int64_t R, int64_t E) { return (size_t)((R + 127) / 128 + E + 1) * 4; }
+// counters of the fused short-batch launch: per m-tile (gate/up stored), then per (m-tile,
+// down n-tile) (y stored)
+size_t ready_bytes(int64_t R, int64_t E, int64_t H) {
+  return (size_t)((R + 127) / 128 + E + 1) * (size_t)(1 + (H + 255) / 256) * 4;
+}
 
 FwdLayout fwd_layout(int64_t T, int64_t E, int64_t H, int64_t I, int k, int ldt, int wdt) {
   const int64_t R = T * k;
@@ -44,7 +48,7 @@ FwdLayout fwd_layout(int64_t T, int64_t E, int64_t H, int64_t I, int k, int ldt,
   l.tor = c.take((size_t)R * 4);
   l.offsets = c.take((size_t)(E + 1) * 4);
   l.hist = c.take(dispatch_scratch_bytes(R, (int)E));
-  l.ready = c.take(ready_bytes(R, E));  // per-m-tile counters of the fused short-batch path
+  l.ready = c.take(ready_bytes(R, E, H));  // per-m-tile counters of the fused short-batch path
   l.xd = c.take((size_t)R * H * dtype_size(wdt));  // x_d, later reused for y
   l.a = c.take((size_t)R * I * dtype_size(wdt));
   l.total = c.off;

@@ -16,7 +16,8 @@
 //   4. down      the same GEMM on a -> y (y reuses the x_d buffer).  No barrier before it: a
 //                per-m-tile count of stored gate/up warps gates the A loads of each down tile,
 //                so the down GEMM starts while the last gate/up tiles are still running.
-//   5. combine   (token, 256-column chunk) items strided over all warps (combine_core.cuh).
+//   5. combine   (token, 256-column chunk) items strided over all warps (combine_core.cuh), each
+//                waiting only for the down tiles it reads (no grid barrier before it).
 // Data written in one phase and read in a later one goes through L2 only: generic loads use
 // ld.global.cg, and x_d / a, which the next phase reads with TMA, are ordered for the async proxy
 // by fence.proxy.async on both sides of the barrier.  Every wait (mbarriers and the grid barrier)
@@ -71,7 +72,8 @@ struct DecodeParams {
   unsigned* grid_count;   // zero at launch
   unsigned* tile_count;   // zeroed in phase 1: GEMM tiles claimed after the static first ones
   unsigned* mtile_ready;  // [n_ready], zeroed in phase 1: stored gate/up warps per m-tile
-  int n_ready;
+                          // [n_mtiles], then stored down warps per (m-tile, n-tile)
+  int n_ready, n_mtiles;
   TcParams gu, dn;        // offsets filled in by the kernel (shared memory)
 };
 
@@ -258,6 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gu.ready_signal = p.mtile_ready;
     dn.ready_wait = p.mtile_ready;
     dn.ready_target = 4u * (unsigned)gu.NT;
+    dn.ready_signal = p.mtile_ready + p.n_mtiles;  // y: per (m-tile, n-tile), for the combine
+    dn.signal_nt = dn.NT;
     const int n_gu = pref[p.E] * gu.NT, total = n_gu + pref[p.E] * dn.NT;
     int q = 0;
     uint32_t ph = 0;
@@ -316,18 +320,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  grid_barrier(p.grid_count, 3, ring.abort_f, p.status);
+  __syncthreads();  // this CTA's GEMM roles are done (no grid barrier: see the combine)
 
   // ---------------------------------------------------------------- 5. combine
+  // Item (token t, 256-column chunk c) reads column tile c of the down GEMM for the k rows of
+  // t: it waits only for those tiles' epilogue warps (a per-(m-tile, n-tile) count), so it can
+  // start while other CTAs still finish their last GEMM tiles.  This CTA got here after the
+  // claim counter ran out, so every tile it may wait for is held by a CTA that completes it.
   if (!*ring.abort_f) {
     const int64_t chunks = (int64_t)p.H * 2 / 16;
-    const int64_t wpt = (chunks + 31) / 32;
+    const int64_t wpt = (chunks + 31) / 32;  // = the down GEMM's n-tiles (256 columns each)
+    const unsigned* y_ready = p.mtile_ready + p.n_mtiles;
     for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < (int64_t)p.T * wpt;
          it += (int64_t)gridDim.x * kWarps) {
       const int64_t t = (uint32_t)it / (uint32_t)wpt;  // 32-bit division (it < T * wpt)
+      const int c = (int)(it - t * wpt);
+      bool ok = true;
+      for (int j = lane; j < p.k; j += 32) {
+        const uint32_t r = ld_cg_u32(p.row_of_slot + t * p.k + j);
+        if (r != kInvalidRow) {
+          const int e = find_expert(offs, p.E, (int)r);  // offs[e] <= r < offs[e + 1]
+          const int gm = pref[e] + ((int)r - offs[e]) / BM;
+          ok &= wait_count(y_ready + (size_t)gm * wpt + c, 4u, ring.abort_f, p.status);
+        }
+      }
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
       combine_warp<TX, TL, true, true, 8>(reinterpret_cast<const TX*>(p.x_d), p.row_of_slot,
-                                       reinterpret_cast<const TL*>(p.w), t, p.H, p.k,
-                                       it - t * wpt, reinterpret_cast<TX*>(p.out), lane);
+                                       reinterpret_cast<const TL*>(p.w), t, p.H, p.k, c,
+                                       reinterpret_cast<TX*>(p.out), lane);
     }
   }
 
@@ -389,7 +409,8 @@ cudaError_t launch_t(const FusedDecodeArgs& f, cudaStream_t s) {
   p.grid_count = f.grid_count;
   p.tile_count = f.tile_count;
   p.mtile_ready = f.mtile_ready;
-  p.n_ready = (int)((R + BM - 1) / BM + f.E + 1);
+  p.n_mtiles = (int)((R + BM - 1) / BM + f.E + 1);
+  p.n_ready = p.n_mtiles * (1 + (f.H + BN - 1) / BN);
   p.gu.out = (uint8_t*)f.a;
   p.gu.status = f.status;
   p.gu.E = f.E;

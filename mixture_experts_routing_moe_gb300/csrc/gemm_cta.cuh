@@ -81,6 +81,7 @@ struct TcParams {
   unsigned* ready_signal;
   const unsigned* ready_wait;
   unsigned ready_target;
+  int signal_nt;  // > 0: ready_signal is per (m-tile, n-tile): index (pref[e] + m) * signal_nt + n
 };
 
 __device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
@@ -356,7 +357,8 @@ __device__ __forceinline__ bool epilogue_tile(const TcParams& p, const int* pref
       mbar_arrive(r.tempty_bar(st.acc));
       if (p.ready_signal) {
         __threadfence();
-        atomicAdd(p.ready_signal + pref[e] + m, 1u);
+        const int gm = pref[e] + m;
+        atomicAdd(p.ready_signal + (p.signal_nt > 0 ? gm * p.signal_nt + n : gm), 1u);
       }
     }
     st.acc ^= 1;

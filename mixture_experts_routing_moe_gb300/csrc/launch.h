@@ -95,7 +95,8 @@ struct FusedDecodeArgs {
   unsigned* status;
   unsigned* grid_count;   // zero at launch
   unsigned* tile_count;   // zeroed by the kernel
-  unsigned* mtile_ready;  // ceil(T k / 128) + E + 1 counters, zeroed by the kernel
+  unsigned* mtile_ready;  // (ceil(T k / 128) + E + 1) x (1 + ceil(H / 256)) counters, zeroed by
+                          // the kernel
 };
 bool fused_decode_supported(int64_t T, int E, int64_t H, int64_t I, int k, int ldt, int wdt);
 cudaError_t launch_decode_fused(const FusedDecodeArgs& f, int ldt, int wdt, cudaStream_t s);
