@@ -511,7 +511,9 @@ def run_sigmoid(args):
                          "frac": gbs / pk["hbm_gbs"], "peak_source": f"{pk_src} HBM copy",
                          "traffic": None, "algorithmic_bytes_per_launch": nbytes},
             "stages_ms": {"route_sigmoid": route_ms, "layer": layer_ms},
-            "gpu_launches": args.steps * (1 + 1 + 4 + 2 + 1), "clocks": clocks}
+            "gpu_launches": args.steps * (1 + (1 if moe.moe_forward_fused(
+                wl.T, wl.E, wl.H, wl.I, wl.top_k, logits.dtype, x.dtype) else kernels_per_forward(wl))),
+            "clocks": clocks}
     print(json.dumps(line), flush=True)
 
 

@@ -235,7 +235,8 @@ int moe_forward_fused(int64_t T, int64_t E, int64_t H, int64_t I, int top_k, int
 /*
  * moe_forward_sigmoid_grouped — SwiGluExperts::forward_sigmoid_grouped of §10: group-limited
  * sigmoid routing (as moe_route_sigmoid_grouped), then dispatch, experts and combine exactly as
- * moe_forward.  Workspace: moe_forward_workspace_bytes(T, E, H, I, top_k, ldt, wdt).
+ * moe_forward, including the single fused launch for the sizes moe_forward_fused reports.
+ * Workspace: moe_forward_workspace_bytes(T, E, H, I, top_k, ldt, wdt).
  */
 int moe_forward_sigmoid_grouped(const void* x, const void* logits, int ldt, const float* bias,
                                 const void* gate, const void* up, const void* down, int wdt,

@@ -114,7 +114,7 @@ bool record(void* const* events, int i, cudaStream_t s) {
 // Whether moe_forward runs the single-launch fused path (softmax routing, no stage events).
 bool takes_fused(const RouteSpec& rs, int64_t T, int64_t E, int64_t H, int64_t I, int top_k,
                  int ldt, int wdt) {
-  if (rs.sigmoid || !valid_dtype(ldt) || !valid_dtype(wdt)) return false;
+  if (!valid_dtype(ldt) || !valid_dtype(wdt)) return false;
   if (E > kFusedDecodeMaxExperts || H > INT32_MAX || I > INT32_MAX) return false;
   if (!fused_decode_supported(T, (int)E, H, I, top_k, ldt, wdt)) return false;
   static int coop[64] = {};  // 1: cooperative launch supported, 2: not (per device)
@@ -178,6 +178,12 @@ int run_forward(const void* x, const void* logits, int ldt, const void* gate, co
     f.I = (int)I;
     f.k = top_k;
     f.renorm = rs.renormalize != 0;
+    f.sigmoid = rs.sigmoid ? 1 : 0;
+    f.bias = rs.bias;
+    f.G = rs.groups;
+    f.SG = rs.selected_groups;
+    f.top_two = rs.top_two != 0;
+    f.scale = rs.scale;
     f.idx = idx;
     f.w = w;
     f.row_of_slot = ros;
@@ -432,7 +438,7 @@ int moe_forward_sigmoid_grouped(const void* x, const void* logits, int ldt, cons
   if (st != MOE_OK) return st;
   const RouteSpec r{true, renormalize, bias, groups, selected_groups, group_top_two, scale};
   return run_forward(x, logits, ldt, gate, up, down, wdt, T, E, H, I, top_k, r, out, ws, ws_bytes,
-                     (cudaStream_t)stream, nullptr, /*allow_fused=*/false);
+                     (cudaStream_t)stream, nullptr, /*allow_fused=*/true);
 }
 
 int moe_combine_backward(const void* y, int ydt, const uint32_t* row_of_slot, const void* w,

@@ -33,6 +33,7 @@
 #include "gemm_cta.cuh"
 #include "launch.h"
 #include "route_core.cuh"
+#include "route_sigmoid_core.cuh"
 #include "tcgen05.cuh"
 
 namespace moe {
@@ -61,6 +62,10 @@ struct DecodeParams {
   const void* gate;       // [E, I, H]
   const void* up;         // [E, I, H]
   int T, E, H, I, k, renorm;
+  // group-limited sigmoid routing (template SIG): bias may be null
+  const float* bias;
+  int G, SG, top_two;
+  float scale;
   uint32_t* idx;          // [T k]
   void* w;                // [T k] in the logits dtype
   uint32_t* row_of_slot;  // [T k]
@@ -105,7 +110,7 @@ __device__ __forceinline__ void grid_barrier(unsigned* count, unsigned n, volati
   __syncthreads();
 }
 
-template <typename TL, bool BF16>
+template <typename TL, bool BF16, bool SIG>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_decode_fused(const __grid_constant__ CUtensorMap map_xd,
                      const __grid_constant__ CUtensorMap map_gate,
@@ -159,7 +164,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) *p.tile_count = 0u;
     for (int i = threadIdx.x; i < p.n_ready; i += blockDim.x) p.mtile_ready[i] = 0u;
   }
-  {
+  if constexpr (SIG) {
+    double* cs = reinterpret_cast<double*>(scratch) + (size_t)warp * (p.E + 128 + 64 + 32);
+    for (int64_t row = (int64_t)blockIdx.x * kWarps + warp; row < p.T;
+         row += (int64_t)gridDim.x * kWarps) {
+      sigmoid_route_row<TL, 8>(reinterpret_cast<const TL*>(p.logits) + row * (int64_t)p.E, p.bias,
+                               row, p.E, p.k, p.G, p.SG, p.top_two, p.renorm, p.scale, cs, lane,
+                               p.idx, reinterpret_cast<TL*>(p.w));
+      __syncwarp();
+    }
+  } else {
     uint32_t* s_id = reinterpret_cast<uint32_t*>(scratch) + warp * p.k;
     float* s_e = reinterpret_cast<float*>(scratch + (size_t)kWarps * p.k * 4) + warp * p.k;
     for (int64_t row = (int64_t)blockIdx.x * kWarps + warp; row < p.T;
@@ -362,9 +376,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <typename TL, bool BF16>
+template <typename TL, bool BF16, bool SIG>
 cudaError_t launch_t(const FusedDecodeArgs& f, cudaStream_t s) {
-  auto kern = moe_decode_fused<TL, BF16>;
+  auto kern = moe_decode_fused<TL, BF16, SIG>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kFusedSmemBytes);
   if (err != cudaSuccess) return err;
@@ -398,6 +412,11 @@ cudaError_t launch_t(const FusedDecodeArgs& f, cudaStream_t s) {
   p.I = f.I;
   p.k = f.k;
   p.renorm = f.renorm;
+  p.bias = f.bias;
+  p.G = f.G;
+  p.SG = f.SG;
+  p.top_two = f.top_two;
+  p.scale = f.scale;
   p.idx = f.idx;
   p.w = f.w;
   p.row_of_slot = f.row_of_slot;
@@ -439,6 +458,19 @@ cudaError_t launch_t(const FusedDecodeArgs& f, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, kern, m_xd, m_gate, m_up, m_a, m_down, p);
 }
 
+template <bool SIG>
+cudaError_t launch_r(const FusedDecodeArgs& f, int ldt, int wdt, cudaStream_t s) {
+  const bool bf = wdt == MOE_BF16;
+  switch (ldt) {
+    case MOE_F32: return bf ? launch_t<float, true, SIG>(f, s) : launch_t<float, false, SIG>(f, s);
+    case MOE_F16: return bf ? launch_t<__half, true, SIG>(f, s) : launch_t<__half, false, SIG>(f, s);
+    case MOE_BF16:
+      return bf ? launch_t<__nv_bfloat16, true, SIG>(f, s)
+                : launch_t<__nv_bfloat16, false, SIG>(f, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 bool fused_decode_supported(int64_t T, int E, int64_t H, int64_t I, int k, int ldt, int wdt) {
@@ -454,14 +486,7 @@ bool fused_decode_supported(int64_t T, int E, int64_t H, int64_t I, int k, int l
 }
 
 cudaError_t launch_decode_fused(const FusedDecodeArgs& f, int ldt, int wdt, cudaStream_t s) {
-  const bool bf = wdt == MOE_BF16;
-  switch (ldt) {
-    case MOE_F32: return bf ? launch_t<float, true>(f, s) : launch_t<float, false>(f, s);
-    case MOE_F16: return bf ? launch_t<__half, true>(f, s) : launch_t<__half, false>(f, s);
-    case MOE_BF16:
-      return bf ? launch_t<__nv_bfloat16, true>(f, s) : launch_t<__nv_bfloat16, false>(f, s);
-  }
-  return cudaErrorInvalidValue;
+  return f.sigmoid ? launch_r<true>(f, ldt, wdt, s) : launch_r<false>(f, ldt, wdt, s);
 }
 
 }  // namespace moe

@@ -85,6 +85,11 @@ struct FusedDecodeArgs {
   const void* down;
   int64_t T;
   int E, H, I, k, renorm;
+  // group-limited sigmoid routing instead of the softmax (bias may be null)
+  int sigmoid;
+  const float* bias;
+  int G, SG, top_two;
+  float scale;
   uint32_t* idx;
   void* w;
   uint32_t* row_of_slot;

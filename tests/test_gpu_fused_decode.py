@@ -96,3 +96,35 @@ def test_fused_path_selection():
     assert not moe.moe_forward_fused(256, 128, 2040, 768, 8, bf, bf)       # H % 64 != 0
     assert not moe.moe_forward_fused(256, 124, 2048, 768, 8, bf, bf)       # E * 2 % 16 != 0
     assert moe.moe_forward_fused(256, 128, 2048, 768, 8, bf, bf)
+
+
+@pytest.mark.parametrize("name,T,E,k,H,I,G,SG,top2", [
+    ("decode_sigmoid", 256, 128, 8, 2048, 768, 8, 4, True),
+    ("small_sigmoid", 60, 96, 4, 256, 192, 6, 2, False),
+])
+def test_fused_sigmoid_forward_equals_stages(name, T, E, k, H, I, G, SG, top2):
+    """moe_forward_sigmoid_grouped on a short batch runs the single fused launch; it equals, bit
+    for bit, the stage calls (sigmoid route, dispatch, experts, combine) on the same inputs, and
+    a sample of tokens matches the oracle."""
+    assert moe.moe_forward_fused(T, E, H, I, k, torch.bfloat16, torch.bfloat16)
+    wl = W.Workload(name, T=T, E=E, top_k=k, renormalize=True, dtype="bf16", seed=23, H=H, I=I,
+                    zipf_s=1.0)
+    g = W.make_layer_inputs(wl, DEV)
+    bias = (0.02 * torch.randn(E, generator=torch.Generator(device=DEV).manual_seed(3),
+                               device=DEV)).float()
+    out = moe.moe_forward_sigmoid_grouped(g["x"], g["logits"], g["gate"], g["up"], g["down"], k, G,
+                                          SG, top2, True, 1.5, bias)
+    idx, w = moe.moe_route_sigmoid_grouped(g["logits"], k, G, SG, top2, True, 1.5, bias)
+    d = moe.moe_dispatch(g["x"], idx, E)
+    y = moe.moe_experts_forward_dispatched(d["x_d"], d["offsets"], g["gate"], g["up"], g["down"])
+    staged = moe.moe_combine(y, d["row_of_slot"], w)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.uint8), staged.view(torch.uint8)), "fused != stages"
+    larr, lname = storage(g["logits"])
+    ridx, rw = O.route_sigmoid_grouped(O.to_f64(larr, lname), bias.double().cpu().numpy(), k, G,
+                                       SG, top2, True, 1.5, lname)
+    tok = np.sort(np.random.default_rng(5).choice(T, min(T, 20), replace=False))
+    xs = O.to_f64(storage(g["x"][torch.from_numpy(tok).to(DEV)])[0], "bf16")
+    ref = O.forward_rows(xs, ridx[tok], rw[tok],
+                         oracle_expert_weights(g["gate"], g["up"], g["down"], "bf16"))
+    assert rel_max_err(f64(out)[tok], ref) <= layer_tol(torch.bfloat16)
