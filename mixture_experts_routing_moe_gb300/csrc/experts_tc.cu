@@ -106,8 +106,10 @@ constexpr int BM2 = 256, STAGES2 = 6;
 constexpr int A2_BYTES = 128 * BK * 2;  // 16 KB
 constexpr int B2_BYTES = 128 * BK * 2;  // 16 KB: half of the 256-row B tile
 constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;
+// down epilogue: one 32-row x 64-column bf16 staging buffer (4 KB) per epilogue warp
+constexpr int kStage2Out = 32 * 128;
 constexpr size_t kSmem2Bytes = 1024 + (size_t)STAGES2 * STAGE2_BYTES + 256 +
-                               (kMaxExperts + 4) * sizeof(int);
+                               (kMaxExperts + 4) * sizeof(int) + 4 * kStage2Out;
 
 template <bool GATEUP, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -128,6 +130,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 5);
   volatile int* abort_f = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* pref = reinterpret_cast<int*>(tmem_slot + 4);
+  // staging of the down epilogue, after the barriers (256 B) and the prefix (kMaxExperts + 4 ints)
+  const uint32_t stage_out =
+      base + STAGES2 * STAGE2_BYTES + 256 + (uint32_t)((kMaxExperts + 4) * sizeof(int));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -302,6 +307,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                   pk[i] = pack2<BF16>(a2[0], a2[1]);
                 }
                 st_v4(orow + (size_t)(col0 + v * 8) * 2, make_uint4(pk[0], pk[1], pk[2], pk[3]));
+              }
+            }
+          }
+        }
+      } else if (!half && __all_sync(0xFFFFFFFFu, valid)) {
+        // full tile, all 32 rows of this warp in the expert: 64-column chunks staged through
+        // shared memory (16-byte chunk j of row r at j ^ (r & 7)) and written as whole 128-byte
+        // lines, 8 lanes per row, instead of one 16-byte piece of 32 different rows per store
+        const uint32_t buf = stage_out + (uint32_t)(q * kStage2Out);
+        const int row0 = r0 + (int)rank * 128 + q * 32;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32], r2[32];
+          tmem_ld32(taddr + c * 64, r);
+          tmem_ld32(taddr + c * 64 + 32, r2);
+          tmem_wait_ld();
+          const int col0 = n * BN + c * 64;
+          if (col0 + 64 <= p.N) {
+            __syncwarp();  // every lane is done reading the previous chunk out of `buf`
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t* src = j < 4 ? r + 8 * j : r2 + 8 * (j - 4);
+              st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4),
+                           pack2<BF16>(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                           pack2<BF16>(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                           pack2<BF16>(__uint_as_float(src[4]), __uint_as_float(src[5])),
+                           pack2<BF16>(__uint_as_float(src[6]), __uint_as_float(src[7])));
+            }
+            __syncwarp();
+#pragma unroll
+            for (int pass = 0; pass < 8; ++pass) {
+              const int rr = pass * 4 + (lane >> 3), ch = lane & 7;
+              const uint4 v = ld_shared_v4(buf + rr * 128 + ((ch ^ (rr & 7)) << 4));
+              st_v4(p.out + ((size_t)(row0 + rr) * p.N + col0 + ch * 8) * 2, v);
+            }
+          } else {  // ragged N: this lane's row, 16 bytes at a time
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const int cc = col0 + v * 8;
+              if (cc < p.N) {
+                const uint32_t* src = v < 4 ? r + 8 * v : r2 + 8 * (v - 4);
+                st_v4(orow + (size_t)cc * 2,
+                      make_uint4(pack2<BF16>(__uint_as_float(src[0]), __uint_as_float(src[1])),
+                                 pack2<BF16>(__uint_as_float(src[2]), __uint_as_float(src[3])),
+                                 pack2<BF16>(__uint_as_float(src[4]), __uint_as_float(src[5])),
+                                 pack2<BF16>(__uint_as_float(src[6]), __uint_as_float(src[7]))));
               }
             }
           }
