@@ -299,6 +299,15 @@ int moe_forward_with_events(const void* x, const void* logits, int ldt, const vo
                             size_t ws_bytes, moe_stream_t stream, void* const* events);
 
 /*
+ * moe_wait_selftest — exercises the failure path of the tensor-core kernels without a fault: one
+ * bounded mbarrier wait (the same routine those kernels use) on a barrier that nothing completes.
+ * It gives up after about a second, sets the timeout bit in the status word at the start of `ws`
+ * (>= 256 bytes, 256-byte aligned) and returns; moe_device_status then reports MOE_ERR_TIMEOUT and
+ * the context stays usable.  For tests and diagnostics; it touches nothing else.
+ */
+int moe_wait_selftest(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_device_status — synchronises `stream`, then reads and clears the status word at the start
  * of a workspace used by moe_dispatch, moe_experts_forward_dispatched or moe_forward.
  * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_INDEX, or MOE_ERR_CUDA if the read itself failed.

@@ -9,4 +9,5 @@ from .binding import (MoeError, moe_combine_backward, moe_dispatch_backward,  # 
                       moe_experts_forward_dispatched, moe_forward, moe_forward_fused,
                       moe_forward_sigmoid_grouped,
                       moe_forward_with_events, moe_route, moe_route_sigmoid_grouped,
-                      moe_selected_router_backward, moe_selected_router_weights)
+                      moe_selected_router_backward, moe_selected_router_weights,
+                      moe_wait_selftest)

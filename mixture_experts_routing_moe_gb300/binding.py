@@ -53,6 +53,7 @@ _SIGS = {
     "moe_forward_with_events": (_int, [_vp, _vp, _int, _vp, _vp, _vp, _int, _i64, _i64, _i64,
                                        _i64, _int, _int, _vp, _vp, _sz, _vp, _vp]),
     "moe_forward_fused": (_int, [_i64, _i64, _i64, _i64, _int, _int, _int]),
+    "moe_wait_selftest": (_int, [_vp, _sz, _vp]),
     "moe_combine_backward": (_int, [_vp, _int, _vp, _vp, _int, _vp, _i64, _i64, _int, _vp, _vp,
                                     _vp]),
     "moe_experts_backward_workspace_bytes": (_sz, [_i64, _i64]),
@@ -370,6 +371,12 @@ def moe_dispatch_backward(dinput, row_of_slot, T: int, top_k: int, stream=None):
     _check(lib().moe_dispatch_backward(_ptr(dinput), _code(dinput), _ptr(row_of_slot), T, H, top_k,
                                        _ptr(dx), _stream(stream)), "moe_dispatch_backward")
     return dx
+
+
+def moe_wait_selftest(ws, stream=None) -> None:
+    """One bounded wait that nothing completes: the timeout lands in ws's status word."""
+    _cuda(ws)
+    _check(lib().moe_wait_selftest(_ptr(ws), ws.numel(), _stream(stream)), "moe_wait_selftest")
 
 
 def moe_device_status(ws, stream=None) -> int:

@@ -409,6 +409,12 @@ int moe_forward(const void* x, const void* logits, int ldt, const void* gate, co
                      (cudaStream_t)stream, nullptr, /*allow_fused=*/true);
 }
 
+int moe_wait_selftest(void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!ws) return MOE_ERR_NULL;
+  if (((uintptr_t)ws & 255u) != 0 || ws_bytes < kWsHeader) return MOE_ERR_WORKSPACE;
+  return cuda_status(launch_wait_selftest((unsigned*)ws, (cudaStream_t)stream));
+}
+
 int moe_forward_fused(int64_t T, int64_t E, int64_t H, int64_t I, int top_k, int ldt, int wdt) {
   if (check_route_shape(T, E, top_k) != MOE_OK || check_experts_shape(T * top_k, E, H, I) != MOE_OK)
     return 0;

@@ -60,6 +60,9 @@ cudaError_t launch_dispatch(const void* x, int xdt, int64_t T, int64_t H, const 
                             uint32_t* row_of_slot, int32_t* hist, unsigned* status,
                             cudaStream_t s);
 
+// One bounded mbarrier wait that nothing completes: sets kStatusTimeout in *status after ~1 s.
+cudaError_t launch_wait_selftest(unsigned* status, cudaStream_t s);
+
 // Device address of that scratch on the current device (looked up on first use per device).
 cudaError_t static_dispatch_scratch(void** ptr);
 

@@ -22,7 +22,7 @@ F32, F16, BF16 = B.MOE_F32, B.MOE_F16, B.MOE_BF16
 
 def test_exports_every_header_function(L):
     names = B.header_functions()
-    assert len(names) == 22
+    assert len(names) == 23
     for n in names:
         assert hasattr(L, n), n
     assert L.moe_abi_version() == 1
@@ -156,6 +156,12 @@ def test_router_train_rejects(L):
     assert fw(T=0, logits=None) == 0
     assert L.moe_selected_router_backward(FAKE, F32, FAKE, 2, None, 8, 16, 4, 1, 0, 1.0, FAKE,
                                           None) == 1
+
+
+def test_wait_selftest_rejects(L):
+    assert L.moe_wait_selftest(None, 256, None) == 1
+    assert L.moe_wait_selftest(FAKE + 16, 256, None) == 5
+    assert L.moe_wait_selftest(FAKE, 255, None) == 5
 
 
 def test_backward_chain_rejects(L):
