@@ -36,32 +36,79 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
 
 // ------------------------------------------------------------------------------------------
 // Fast path for 16-bit logits with E <= 64 (E % 8 == 0, 16-byte aligned rows) and top_k <= 8:
-// one row per thread.  Keys are 32-bit: monotone 16-bit value bits << 16 | (0xFFFF - id), so a
-// larger key is a larger logit and equal logits prefer the lower id.  Each 16-byte vector (8
-// experts) is sorted by an 8-input sorting network and merged into the running sorted top 8 with
-// a bitonic merge (elementwise max against the reversed list, then a half-cleaner).  The softmax
-// denominator is accumulated online over the vectors (rescaled when the running max grows);
-// with renormalisation only the selected experts' exponentials are needed.
-__device__ __forceinline__ void ce_desc(uint32_t& a, uint32_t& b) {
-  const uint32_t hi = max(a, b), lo = min(a, b);
-  a = hi;
-  b = lo;
+// one row per thread.
+//
+// Ranking.  A larger logit ranks first, equal logits prefer the lower id.  Most rows are decided
+// on half-width keys: with m the row's largest value,
+//     key16 = d << 6 | id,   d = min(number of 16-bit codes from the value up to m, 1023),
+// smaller first.  The 1023 codes below m keep their exact order and every lower value is squashed
+// into d = 1023.  d comes straight from the storage bits: when m is positive (bits >= 1023 as a
+// signed 16-bit integer) the non-negative values in the window are ordered like their bits, and a
+// signed packed max against m - 1023 clamps everything lower (every negative value included); when
+// m is negative every value is, and flipping all bits turns them into the same case.  Two keys
+// share a register (even expert in the low half, odd in the high half) and the packed min / max
+// (min.u16x2) runs the sorting networks on both halves at once: each 8-word group is two
+// independent 8-input sorts, the groups merge into two sorted top-8 lists (elementwise min against
+// the reversed list, then a half-cleaner), and a last merge of the low half against the high half
+// leaves the row's top 8.  When the 8th key has d < 1023, every chosen key lies in the window,
+// where the order is exact, and every key not chosen is below it.  Otherwise (the top 8 span more
+// than 1023 codes, e.g. -inf among them), and for rows whose largest value is a zero or tiny, the
+// row is decided again on exact 32-bit keys: monotone code << 16 | (0xFFFF - id), larger first.
+__device__ __forceinline__ uint32_t vmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
-__device__ __forceinline__ void sort8_desc(uint32_t (&k)[8]) {
-  ce_desc(k[0], k[1]); ce_desc(k[2], k[3]); ce_desc(k[4], k[5]); ce_desc(k[6], k[7]);
-  ce_desc(k[0], k[2]); ce_desc(k[1], k[3]); ce_desc(k[4], k[6]); ce_desc(k[5], k[7]);
-  ce_desc(k[1], k[2]); ce_desc(k[5], k[6]);
-  ce_desc(k[0], k[4]); ce_desc(k[1], k[5]); ce_desc(k[2], k[6]); ce_desc(k[3], k[7]);
-  ce_desc(k[2], k[4]); ce_desc(k[3], k[5]);
-  ce_desc(k[1], k[2]); ce_desc(k[3], k[4]); ce_desc(k[5], k[6]);
+__device__ __forceinline__ uint32_t vmin2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
-// top: sorted descending; g: sorted descending.  Leaves the 8 largest of both in `top`, sorted.
-__device__ __forceinline__ void merge_top8(uint32_t (&top)[8], const uint32_t (&g)[8]) {
+__device__ __forceinline__ uint32_t vmax2s(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.s16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// packed floating-point max of both halves; a NaN in either operand gives NaN
+template <typename T>
+__device__ __forceinline__ uint32_t fmax2_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  if constexpr (Dt<T>::code == MOE_BF16) {
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  } else {
+    asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  }
+  return d;
+}
+// compare-exchange: ASC = smaller first on packed 16-bit halves, else larger first on 32-bit keys
+template <bool ASC>
+__device__ __forceinline__ void cx(uint32_t& a, uint32_t& b) {
+  const uint32_t f = ASC ? vmin2(a, b) : max(a, b), s = ASC ? vmax2(a, b) : min(a, b);
+  a = f;
+  b = s;
+}
+template <bool ASC>
+__device__ __forceinline__ void sort8(uint32_t (&k)[8]) {
+  cx<ASC>(k[0], k[1]); cx<ASC>(k[2], k[3]); cx<ASC>(k[4], k[5]); cx<ASC>(k[6], k[7]);
+  cx<ASC>(k[0], k[2]); cx<ASC>(k[1], k[3]); cx<ASC>(k[4], k[6]); cx<ASC>(k[5], k[7]);
+  cx<ASC>(k[1], k[2]); cx<ASC>(k[5], k[6]);
+  cx<ASC>(k[0], k[4]); cx<ASC>(k[1], k[5]); cx<ASC>(k[2], k[6]); cx<ASC>(k[3], k[7]);
+  cx<ASC>(k[2], k[4]); cx<ASC>(k[3], k[5]);
+  cx<ASC>(k[1], k[2]); cx<ASC>(k[3], k[4]); cx<ASC>(k[5], k[6]);
+}
+// bitonic sequence of 8 -> sorted
+template <bool ASC>
+__device__ __forceinline__ void clean8(uint32_t (&t)[8]) {
+  cx<ASC>(t[0], t[4]); cx<ASC>(t[1], t[5]); cx<ASC>(t[2], t[6]); cx<ASC>(t[3], t[7]);
+  cx<ASC>(t[0], t[2]); cx<ASC>(t[1], t[3]); cx<ASC>(t[4], t[6]); cx<ASC>(t[5], t[7]);
+  cx<ASC>(t[0], t[1]); cx<ASC>(t[2], t[3]); cx<ASC>(t[4], t[5]); cx<ASC>(t[6], t[7]);
+}
+// top, g: sorted.  Leaves the 8 best of both in `top`, sorted.
+template <bool ASC>
+__device__ __forceinline__ void merge8(uint32_t (&top)[8], const uint32_t (&g)[8]) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) top[i] = max(top[i], g[7 - i]);  // bitonic, holds the top 8
-  ce_desc(top[0], top[4]); ce_desc(top[1], top[5]); ce_desc(top[2], top[6]); ce_desc(top[3], top[7]);
-  ce_desc(top[0], top[2]); ce_desc(top[1], top[3]); ce_desc(top[4], top[6]); ce_desc(top[5], top[7]);
-  ce_desc(top[0], top[1]); ce_desc(top[2], top[3]); ce_desc(top[4], top[5]); ce_desc(top[6], top[7]);
+  for (int i = 0; i < 8; ++i) top[i] = ASC ? vmin2(top[i], g[7 - i]) : max(top[i], g[7 - i]);
+  clean8<ASC>(top);
 }
 template <typename T>
 __device__ __forceinline__ float bits16_to_float(uint32_t b) {
@@ -71,102 +118,231 @@ __device__ __forceinline__ float bits16_to_float(uint32_t b) {
     return __half2float(__ushort_as_half((unsigned short)b));
   }
 }
+// the storage bits of a 16-bit value
+template <typename T>
+__device__ __forceinline__ uint32_t bits16(T v) {
+  if constexpr (Dt<T>::code == MOE_BF16) {
+    return __bfloat16_as_ushort(v);
+  } else {
+    return __half_as_ushort(v);
+  }
+}
+
+// Weights of the chosen experts (ids, storage bits of their logits) and the stores of one row.
+template <typename T, bool RENORM>
+__device__ __forceinline__ void emit_row(uint32_t (&id)[8], const uint32_t (&vb)[8], bool poisoned,
+                                         float x0, float sum, int k, int vec_store,
+                                         uint32_t* __restrict__ idx_out, T* __restrict__ w_out,
+                                         int64_t row) {
+  float ex[8], sel = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    ex[j] = __expf(bits16_to_float<T>(vb[j]) - x0);
+    if (j < k) sel += ex[j];
+  }
+  const float inv = 1.f / (RENORM ? sel : sum);
+  float wt[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    id[j] = poisoned ? (uint32_t)j : id[j];
+    wt[j] = poisoned ? __int_as_float(0x7FC00000) : ex[j] * inv;
+  }
+  if (vec_store) {  // k == 8, 16-byte aligned outputs
+    uint4* io = reinterpret_cast<uint4*>(idx_out + row * 8);
+    io[0] = make_uint4(id[0], id[1], id[2], id[3]);
+    io[1] = make_uint4(id[4], id[5], id[6], id[7]);
+    uint32_t p[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      p[j] = bits16<T>(Dt<T>::from_f(wt[2 * j])) | (bits16<T>(Dt<T>::from_f(wt[2 * j + 1])) << 16);
+    *reinterpret_cast<uint4*>(w_out + row * 8) = make_uint4(p[0], p[1], p[2], p[3]);
+  } else {
+    uint32_t* io = idx_out + row * k;
+    T* wo = w_out + row * k;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j < k) {
+        io[j] = id[j];
+        wo[j] = Dt<T>::from_f(wt[j]);
+      }
+    }
+  }
+}
+
+// A row decided on exact 32-bit keys (monotone code << 16 | (0xFFFF - id), larger first): every
+// f16 row, and the bf16 rows whose top 8 reach below the half-width window or whose largest value
+// is a zero or tiny (for those it is called out of line, so that the common path holds no
+// registers for it).  Vector v of the row is rowv[v ^ sw] (shared or global memory).
+template <typename T, int NV, bool RENORM>
+__device__ __forceinline__ void exact_row(const uint4* rowv, int sw, float x0, float sum, int k,
+                                          int vec_store, uint32_t* idx_out, T* w_out,
+                                          int64_t row) {
+  uint32_t top[8];
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const uint4 q = rowv[v ^ sw];
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    uint32_t g[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // monotone code of both halves: negative -> all bits flipped, else sign bit set; prmt
+      // with selector 0xBB99 replicates each half's sign bit over the half
+      uint32_t sm;
+      asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(sm) : "r"(w[i]));
+      const uint32_t m = w[i] ^ (sm | 0x80008000u);
+      const uint32_t e0 = v * 8 + i * 2;
+      g[2 * i] = (m << 16) | (0xFFFFu - e0);
+      g[2 * i + 1] = (m & 0xFFFF0000u) | (0xFFFFu - (e0 + 1));
+    }
+    sort8<false>(g);
+    if (v == 0) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) top[i] = g[i];
+    } else {
+      merge8<false>(top, g);
+    }
+  }
+  uint32_t id[8], vb[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t t = top[j] >> 16;
+    id[j] = 0xFFFFu - (top[j] & 0xFFFFu);
+    vb[j] = (t & 0x8000u) ? (t & 0x7FFFu) : (~t & 0xFFFFu);
+  }
+  emit_row<T, RENORM>(id, vb, false, x0, sum, k, vec_store, idx_out, w_out, row);
+}
+template <typename T, int NV, bool RENORM>
+__device__ __noinline__ void exact_row_outlined(const uint4* rowv, int sw, float x0, float sum,
+                                                int k, int vec_store, uint32_t* idx_out,
+                                                T* w_out, int64_t row) {
+  exact_row<T, NV, RENORM>(rowv, sw, x0, sum, k, vec_store, idx_out, w_out, row);
+}
 
 template <typename T, int NV, bool RENORM>
-__global__ void __launch_bounds__(256)
-    moe_route16_small(const uint4* __restrict__ logits, int64_t T_, int k,
+__global__ void __launch_bounds__(256, RENORM ? 5 : 4)
+    moe_route16_small(const uint4* __restrict__ logits, int64_t T_, int k, int vec_store,
                       uint32_t* __restrict__ idx_out, T* __restrict__ w_out) {
   constexpr uint32_t EXPMASK = Dt<T>::code == MOE_BF16 ? 0x7F80u : 0x7C00u;
+  constexpr int NG = (NV + 1) / 2;  // groups of 8 words (16 experts)
+  // half-width keys for bf16 only: f16's 10-bit mantissa puts a single binade in the window
+  constexpr bool HALF = Dt<T>::code == MOE_BF16;
+  const int tid = threadIdx.x;
   const int64_t row0 = (int64_t)blockIdx.x * 256;
-  const int64_t row = row0 + threadIdx.x;
+  const int64_t row = row0 + tid;
   // E = 64: the block's 256 rows (32 KB, contiguous) are read with coalesced 16-byte loads into
   // shared memory, vector v of row r stored at slot v ^ (r & 7) so that the row-per-thread reads
-  // below hit 8 different bank groups per 8 lanes.
+  // below hit 8 different bank groups per 8 lanes.  Chunk c = tid + 256 i belongs to row c / 8,
+  // whose low three bits are those of tid / 8, so its slot is c ^ ((tid / 8) & 7).
   constexpr bool STAGED = NV == 8;
   __shared__ uint4 tile[STAGED ? 256 * 8 : 1];
   if (STAGED) {
     const int64_t left = T_ - row0;
     const int n = (int)((left < 256 ? left : 256) * 8);
-    const uint4* bsrc = logits + row0 * 8;
+    const uint4* bsrc = logits + row0 * 8 + tid;
+    uint4* dst = tile + (tid ^ ((tid >> 3) & 7));
+    if (n == 2048) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int c = threadIdx.x + i * 256;
-      if (c < n) tile[(c & ~7) | ((c & 7) ^ ((c >> 3) & 7))] = ld_nc_v4(bsrc + c);
+      for (int i = 0; i < 8; ++i) dst[i * 256] = ld_nc_v4(bsrc + i * 256);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (tid + i * 256 < n) dst[i * 256] = ld_nc_v4(bsrc + i * 256);
     }
     __syncthreads();
   }
   if (row >= T_) return;
   const uint4* src = logits + row * NV;
-  uint32_t top[8];
-  uint32_t rawmax = 0u;  // per-half unsigned max of the raw bits: above -inf only for a negative NaN
-  float m = -INFINITY, s = 0.f;
+  auto load = [&](int v) -> uint4 {
+    return STAGED ? tile[tid * 8 + (v ^ (tid & 7))] : ld_nc_v4(src + v);
+  };
+
+  // pass 1: the row maximum, NaN-propagating
+  uint32_t wv[NG * 8];
+  uint32_t fm = 0u;
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
-    const uint4 q = STAGED ? tile[threadIdx.x * 8 + (v ^ (threadIdx.x & 7))] : ld_nc_v4(src + v);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    const uint4 q = load(v);
+    wv[4 * v] = q.x; wv[4 * v + 1] = q.y; wv[4 * v + 2] = q.z; wv[4 * v + 3] = q.w;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) fm = v == 0 && i == 0 ? wv[0] : fmax2_nan<T>(fm, wv[4 * v + i]);
+  }
+  const uint32_t mb = fmax2_nan<T>(fm, fm >> 16) & 0xFFFFu;  // storage bits of the maximum
+  // poisoned: the maximum is NaN (a NaN anywhere) or +inf, or -inf (every value is -inf)
+  const bool poisoned = (mb & 0x7FFFu) >= EXPMASK;
+  const bool pos = mb >= 1023u && mb < 0x8000u;          // positive maximum, window all >= 0
+  const bool neg = mb > 0x8000u && mb <= 0xFC00u;        // negative maximum, so is every value
+  const float x0 = bits16_to_float<T>(mb);
+  float sum = 0.f;
+  if (!RENORM) {  // softmax denominator over all experts, against the row maximum
+#pragma unroll
+    for (int j = 0; j < NV * 4; ++j) {
+      sum += __expf(bits16_to_float<T>(wv[j] & 0xFFFFu) - x0);
+      sum += __expf(bits16_to_float<T>(wv[j] >> 16) - x0);
+    }
+  }
+
+  const uint4* rowv = STAGED ? tile + tid * 8 : src;
+  const int sw = STAGED ? (tid & 7) : 0;
+  if (poisoned) {
+    uint32_t id[8] = {0, 0, 0, 0, 0, 0, 0, 0}, vb[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    emit_row<T, RENORM>(id, vb, true, x0, sum, k, vec_store, idx_out, w_out, row);
+    return;
+  }
+  if constexpr (!HALF) {
+    exact_row<T, NV, RENORM>(rowv, sw, x0, sum, k, vec_store, idx_out, w_out, row);
+    return;
+  }
+  if (!(pos || neg)) {
+    exact_row_outlined<T, NV, RENORM>(rowv, sw, x0, sum, k, vec_store, idx_out, w_out, row);
+    return;
+  }
+
+  // pass 2: half-width keys d << 6 | id, two per register
+  if (neg) {
+#pragma unroll
+    for (int j = 0; j < NV * 4; ++j) wv[j] = ~wv[j];
+  }
+  const uint32_t mf = neg ? (mb ^ 0xFFFFu) : mb;  // maximum in the (flipped) bit order
+  const uint32_t floor2 = (mf - 1023u) * 0x10001u, m2 = mf * 0x10001u;
+#pragma unroll
+  for (int j = 0; j < NV * 4; ++j)
+    wv[j] = (m2 - vmax2s(wv[j], floor2)) * 64u + ((uint32_t)(2 * j + 1) << 16 | (uint32_t)(2 * j));
+#pragma unroll
+  for (int j = NV * 4; j < NG * 8; ++j) wv[j] = 0xFFFFFFFFu;  // padding after every real key
+  uint32_t top[8];
+#pragma unroll
+  for (int gi = 0; gi < NG; ++gi) {
     uint32_t g[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      // monotone map of both 16-bit halves: negative -> all bits flipped, else sign bit set.
-      // prmt with selector 0xBB99 replicates each half's sign bit over the half (0xFFFF / 0).
-      uint32_t sm;
-      asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(sm) : "r"(w[i]));
-      const uint32_t t = w[i] ^ (sm | 0x80008000u);
-      rawmax = __vmaxu2(rawmax, w[i]);
-      const uint32_t e0 = v * 8 + i * 2;
-      g[2 * i] = (t << 16) | (0xFFFFu - e0);
-      g[2 * i + 1] = (t & 0xFFFF0000u) | (0xFFFFu - (e0 + 1));
-    }
-    if (!RENORM) {  // online softmax denominator
-      float x[8], gm = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[2 * i] = bits16_to_float<T>(w[i] & 0xFFFFu);
-        x[2 * i + 1] = bits16_to_float<T>(w[i] >> 16);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) gm = fmaxf(gm, x[i]);
-      const float mn = fmaxf(m, gm);
-      const float ref = mn == -INFINITY ? 0.f : mn;  // all -inf so far: every term is 0
-      float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc += __expf(x[i] - ref);
-      s = (m == -INFINITY ? 0.f : s * __expf(m - mn)) + acc;
-      m = mn;
-    }
-    sort8_desc(g);
-    if (v == 0) {
+    for (int i = 0; i < 8; ++i) g[i] = wv[8 * gi + i];
+    sort8<true>(g);
+    if (gi == 0) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) top[i] = g[i];
     } else {
-      merge_top8(top, g);
+      merge8<true>(top, g);
     }
   }
-  // poisoned: largest value NaN / +inf / -inf (the last means every value is -inf), or a
-  // negative NaN anywhere (its raw bits exceed those of -inf)
-  const uint32_t tb = top[0] >> 16;
-  const uint32_t vb0 = (tb & 0x8000u) ? (tb & 0x7FFFu) : (~tb & 0xFFFFu);
-  const uint32_t rmax = max(rawmax & 0xFFFFu, rawmax >> 16);  // negative NaN: above 0x8000|EXPMASK
-  const bool poisoned = (vb0 & 0x7FFFu) >= EXPMASK || rmax > (0x8000u | EXPMASK);
-  const float x0 = bits16_to_float<T>(vb0);
-  float ex[8], sel = 0.f;
+  {  // low half (even experts) against the reversed high half (odd experts)
+    uint32_t r[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) asm("prmt.b32 %0, %1, 0, 0x1032;" : "=r"(r[i]) : "r"(top[7 - i]));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) top[i] = vmin2(top[i], r[i]);
+    clean8<true>(top);
+  }
+  if ((top[7] & 0xFFFFu) >= 1023u * 64u) {  // the 8th key squashed: decide again exactly
+    exact_row_outlined<T, NV, RENORM>(rowv, sw, x0, sum, k, vec_store, idx_out, w_out, row);
+    return;
+  }
+  uint32_t id[8], vb[8];  // chosen ids and their storage bits
+  const uint32_t fl = neg ? 0xFFFFu : 0u;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const uint32_t b = top[j] >> 16;
-    const uint32_t vb = (b & 0x8000u) ? (b & 0x7FFFu) : (~b & 0xFFFFu);
-    ex[j] = __expf(bits16_to_float<T>(vb) - x0);
-    if (j < k) sel += ex[j];
+    id[j] = top[j] & 63u;
+    vb[j] = (mf - ((top[j] & 0xFFFFu) >> 6)) ^ fl;
   }
-  const float denom = RENORM ? sel : s * __expf(m - x0);
-  uint32_t* io = idx_out + row * k;
-  T* wo = w_out + row * k;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (j < k) {
-      io[j] = poisoned ? (uint32_t)j : 0xFFFFu - (top[j] & 0xFFFFu);
-      wo[j] = Dt<T>::from_f(poisoned ? __int_as_float(0x7FC00000) : ex[j] / denom);
-    }
-  }
+  emit_row<T, RENORM>(id, vb, false, x0, sum, k, vec_store, idx_out, w_out, row);
 }
 
 template <typename T>
@@ -174,12 +350,13 @@ cudaError_t launch_route16_small(const void* logits, int64_t T_, int E, int k, i
                                  uint32_t* idx, void* w, cudaStream_t s) {
   const unsigned blocks = (unsigned)((T_ + 255) / 256);
   const uint4* l = (const uint4*)logits;
+  const int vst = k == 8 && ((uintptr_t)idx % 16) == 0 && ((uintptr_t)w % 16) == 0;
 #define MOE_R16(NV)                                                                             \
   case NV:                                                                                      \
     if (renorm)                                                                                 \
-      moe_route16_small<T, NV, true><<<blocks, 256, 0, s>>>(l, T_, k, idx, (T*)w);              \
+      moe_route16_small<T, NV, true><<<blocks, 256, 0, s>>>(l, T_, k, vst, idx, (T*)w);         \
     else                                                                                        \
-      moe_route16_small<T, NV, false><<<blocks, 256, 0, s>>>(l, T_, k, idx, (T*)w);             \
+      moe_route16_small<T, NV, false><<<blocks, 256, 0, s>>>(l, T_, k, vst, idx, (T*)w);        \
     break;
   switch (E / 8) {
     MOE_R16(1) MOE_R16(2) MOE_R16(3) MOE_R16(4) MOE_R16(5) MOE_R16(6) MOE_R16(7) MOE_R16(8)

@@ -69,6 +69,60 @@ def test_route_unaligned_rows_take_scalar_path():
     check_weights(w, rw, "unaligned")
 
 
+def _raw16(t):
+    """16-bit storage bits from the monotone code t (sign bit set: non-negative value)."""
+    t = np.asarray(t, dtype=np.int64)
+    return np.where(t & 0x8000, t & 0x7FFF, ~t & 0xFFFF).astype(np.uint16)
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("k", [8, 3])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_route_half_width_boundary(dt, k, renorm):
+    """E = 64 rows built in the monotone code t, around the 1024 codes below each row's largest
+    value that the one-row-per-thread route ranks on half-width keys: the k-th largest exactly
+    1022 or 1023 codes below the top (the last kept code and the first squashed one), ties at
+    that place, equal values straddling the k-th place, and rows spread over many binades."""
+    rng = np.random.default_rng(11 + k)
+    E, T, top = 64, 512, 0xC100                    # top: 8.0 (bf16) / 2.5 (f16)
+    t = np.zeros((T, E), dtype=np.int64)
+    for r in range(T):
+        kind = r % 8
+        row = top - 1100 - rng.integers(0, 3000, E)          # every other value well below
+        perm = rng.permutation(E)
+        row[perm[0]] = top
+        near = perm[1:k]
+        row[near] = top - rng.integers(0, 1022, len(near))
+        if kind == 0:
+            row[perm[k - 1]] = top - 1023                     # k-th squashed: decided again
+        elif kind == 1:
+            row[perm[k - 1]] = top - 1022                     # k-th keeps code 1
+            row[perm[k]] = top - 1023
+        elif kind == 2:
+            row[perm[k - 1]] = row[perm[k]] = top - 1022      # tie across the k-th place
+        elif kind == 3:
+            row[perm[k - 1:k + 3]] = top - 1023               # ties among squashed codes
+        elif kind == 4:
+            row[perm[k - 1]] = row[perm[k]] = top - 500       # tie above the boundary
+        elif kind == 5:
+            row = top - rng.integers(0, 40000, E)             # many binades, both signs
+            row[perm[0]] = top
+        elif kind == 6:
+            row[perm[1:k + 2]] = top                          # all of the top k equal
+        else:
+            row = top - 1022 + rng.integers(0, 1023, E)       # everything inside the window
+        t[r] = row
+    raw = _raw16(t)
+    l = torch.from_numpy(raw.view(np.int16)).view(dt)
+    assert torch.isfinite(l.float()).all()
+    idx, w = moe.moe_route(l.to(DEV), k, renorm)
+    torch.cuda.synchronize()
+    arr, name = storage(l)
+    ridx, rw = O.route(O.to_f64(arr, name), k, renorm, name)
+    np.testing.assert_array_equal(u32(idx), ridx)
+    check_weights(w, rw, f"half-width boundary {name} k={k}")
+
+
 @pytest.mark.parametrize("renorm", [True, False])
 def test_route_sweep_full_size(renorm):
     """The routing-only workload at full size: [1 048 576, 64] bf16, N(0, 2^2), top_k = 8."""
