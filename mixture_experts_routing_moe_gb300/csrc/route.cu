@@ -118,6 +118,12 @@ __device__ __forceinline__ float bits16_to_float(uint32_t b) {
     return __half2float(__ushort_as_half((unsigned short)b));
   }
 }
+// 2^y (PTX ex2.approx, subnormal results flushed to zero)
+__device__ __forceinline__ float ex2_ftz(float y) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+  return r;
+}
 // the storage bits of a 16-bit value
 template <typename T>
 __device__ __forceinline__ uint32_t bits16(T v) {
@@ -273,12 +279,18 @@ __global__ void __launch_bounds__(256, RENORM ? 5 : 4)
   const bool neg = mb > 0x8000u && mb <= 0xFC00u;        // negative maximum, so is every value
   const float x0 = bits16_to_float<T>(mb);
   float sum = 0.f;
-  if (!RENORM) {  // softmax denominator over all experts, against the row maximum
+  if (!RENORM) {
+    // softmax denominator over all experts against the row maximum: exp(x - x0) = 2^(x log2 e -
+    // x0 log2 e).  Terms below 2^-126 are flushed to zero, which leaves the sum (>= 1, the
+    // maximum's own term) unchanged.
+    const float c = x0 * 1.4426950408889634f;
+    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
     for (int j = 0; j < NV * 4; ++j) {
-      sum += __expf(bits16_to_float<T>(wv[j] & 0xFFFFu) - x0);
-      sum += __expf(bits16_to_float<T>(wv[j] >> 16) - x0);
+      s0 += ex2_ftz(fmaf(bits16_to_float<T>(wv[j] & 0xFFFFu), 1.4426950408889634f, -c));
+      s1 += ex2_ftz(fmaf(bits16_to_float<T>(wv[j] >> 16), 1.4426950408889634f, -c));
     }
+    sum = s0 + s1;
   }
 
   const uint4* rowv = STAGED ? tile + tid * 8 : src;
