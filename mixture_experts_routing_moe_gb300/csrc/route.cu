@@ -118,11 +118,18 @@ __device__ __forceinline__ float bits16_to_float(uint32_t b) {
     return __half2float(__ushort_as_half((unsigned short)b));
   }
 }
+constexpr float kLog2e = 1.4426950408889634f;
 // 2^y (PTX ex2.approx, subnormal results flushed to zero)
 __device__ __forceinline__ float ex2_ftz(float y) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
   return r;
+}
+// exp(d) for d <= 0 as (2^(d log2 e / 2))^2: the half power stays normal down to d log2 e = -252,
+// and the square (an IEEE multiply) rounds into the subnormal range where the result lies there
+__device__ __forceinline__ float exp_nonpos(float d) {
+  const float h = ex2_ftz(d * (0.5f * kLog2e));
+  return h * h;
 }
 // the storage bits of a 16-bit value
 template <typename T>
@@ -134,16 +141,16 @@ __device__ __forceinline__ uint32_t bits16(T v) {
   }
 }
 
-// Weights of the chosen experts (ids, storage bits of their logits) and the stores of one row.
+// Weights of the chosen experts (ids, logits) and the stores of one row.
 template <typename T, bool RENORM>
-__device__ __forceinline__ void emit_row(uint32_t (&id)[8], const uint32_t (&vb)[8], bool poisoned,
+__device__ __forceinline__ void emit_row(uint32_t (&id)[8], const float (&x)[8], bool poisoned,
                                          float x0, float sum, int k, int vec_store,
                                          uint32_t* __restrict__ idx_out, T* __restrict__ w_out,
                                          int64_t row) {
   float ex[8], sel = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    ex[j] = __expf(bits16_to_float<T>(vb[j]) - x0);
+    ex[j] = exp_nonpos(x[j] - x0);
     if (j < k) sel += ex[j];
   }
   const float inv = 1.f / (RENORM ? sel : sum);
@@ -208,14 +215,15 @@ __device__ __forceinline__ void exact_row(const uint4* rowv, int sw, float x0, f
       merge8<false>(top, g);
     }
   }
-  uint32_t id[8], vb[8];
+  uint32_t id[8];
+  float x[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const uint32_t t = top[j] >> 16;
     id[j] = 0xFFFFu - (top[j] & 0xFFFFu);
-    vb[j] = (t & 0x8000u) ? (t & 0x7FFFu) : (~t & 0xFFFFu);
+    x[j] = bits16_to_float<T>((t & 0x8000u) ? (t & 0x7FFFu) : (~t & 0xFFFFu));
   }
-  emit_row<T, RENORM>(id, vb, false, x0, sum, k, vec_store, idx_out, w_out, row);
+  emit_row<T, RENORM>(id, x, false, x0, sum, k, vec_store, idx_out, w_out, row);
 }
 template <typename T, int NV, bool RENORM>
 __device__ __noinline__ void exact_row_outlined(const uint4* rowv, int sw, float x0, float sum,
@@ -280,15 +288,14 @@ __global__ void __launch_bounds__(256, RENORM ? 5 : 4)
   const float x0 = bits16_to_float<T>(mb);
   float sum = 0.f;
   if (!RENORM) {
-    // softmax denominator over all experts against the row maximum: exp(x - x0) = 2^(x log2 e -
-    // x0 log2 e).  Terms below 2^-126 are flushed to zero, which leaves the sum (>= 1, the
-    // maximum's own term) unchanged.
-    const float c = x0 * 1.4426950408889634f;
+    // softmax denominator over all experts against the row maximum, exp(x - x0) = 2^((x - x0)
+    // log2 e).  Terms below 2^-126 are flushed to zero, which leaves the sum (>= 1, the maximum's
+    // own term) unchanged.
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
     for (int j = 0; j < NV * 4; ++j) {
-      s0 += ex2_ftz(fmaf(bits16_to_float<T>(wv[j] & 0xFFFFu), 1.4426950408889634f, -c));
-      s1 += ex2_ftz(fmaf(bits16_to_float<T>(wv[j] >> 16), 1.4426950408889634f, -c));
+      s0 += ex2_ftz((bits16_to_float<T>(wv[j] & 0xFFFFu) - x0) * kLog2e);
+      s1 += ex2_ftz((bits16_to_float<T>(wv[j] >> 16) - x0) * kLog2e);
     }
     sum = s0 + s1;
   }
@@ -296,8 +303,9 @@ __global__ void __launch_bounds__(256, RENORM ? 5 : 4)
   const uint4* rowv = STAGED ? tile + tid * 8 : src;
   const int sw = STAGED ? (tid & 7) : 0;
   if (poisoned) {
-    uint32_t id[8] = {0, 0, 0, 0, 0, 0, 0, 0}, vb[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    emit_row<T, RENORM>(id, vb, true, x0, sum, k, vec_store, idx_out, w_out, row);
+    uint32_t id[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    const float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    emit_row<T, RENORM>(id, x, true, x0, sum, k, vec_store, idx_out, w_out, row);
     return;
   }
   if constexpr (!HALF) {
@@ -347,14 +355,17 @@ __global__ void __launch_bounds__(256, RENORM ? 5 : 4)
     exact_row_outlined<T, NV, RENORM>(rowv, sw, x0, sum, k, vec_store, idx_out, w_out, row);
     return;
   }
-  uint32_t id[8], vb[8];  // chosen ids and their storage bits
-  const uint32_t fl = neg ? 0xFFFFu : 0u;
+  // chosen ids, and their logits: bf16 bits ((mf - d) ^ flip) << 16 = (mf << 16) - (d << 16)
+  // ^ (flip << 16), with d << 16 = (key & 0xFFC0) << 10
+  uint32_t id[8];
+  float x[8];
+  const uint32_t m16 = mf << 16, fl16 = neg ? 0xFFFF0000u : 0u;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     id[j] = top[j] & 63u;
-    vb[j] = (mf - ((top[j] & 0xFFFFu) >> 6)) ^ fl;
+    x[j] = __uint_as_float((m16 - (top[j] & 0xFFC0u) * 1024u) ^ fl16);
   }
-  emit_row<T, RENORM>(id, vb, false, x0, sum, k, vec_store, idx_out, w_out, row);
+  emit_row<T, RENORM>(id, x, false, x0, sum, k, vec_store, idx_out, w_out, row);
 }
 
 template <typename T>

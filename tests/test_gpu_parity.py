@@ -123,6 +123,40 @@ def test_route_half_width_boundary(dt, k, renorm):
     check_weights(w, rw, f"half-width boundary {name} k={k}")
 
 
+@pytest.mark.parametrize("dt,scales", [(torch.bfloat16, [300.0, -300.0, 1e6, 1e20, 1e30, -1e30]),
+                                       (torch.float16, [300.0, -300.0, 3e4, -3e4])])
+@pytest.mark.parametrize("E,k", [(64, 8), (40, 5), (128, 8)])
+@pytest.mark.parametrize("renorm", [True, False])
+def test_route_large_logits(dt, scales, E, k, renorm):
+    """Logits of large magnitude: the softmax is taken against the row maximum, so exp(x - x0)
+    must not lose x0's own term.  Rows hold up to four copies of the maximum (weights 1/m) and
+    values a few spacings below it (nonzero weights), at magnitudes up to 1e30 (bf16) and 3e4
+    (f16)."""
+    g = torch.Generator().manual_seed(E * 7 + k)
+    rows = []
+    for i in range(96 * len(scales)):
+        s = scales[i % len(scales)]
+        x0 = torch.tensor(s).to(dt).float()
+        spacing = (torch.tensor(abs(s)).to(dt).float().item()) * (2.0 ** -7 if dt == torch.bfloat16
+                                                                   else 2.0 ** -10)
+        steps = torch.randint(1, 6, (E,), generator=g).float()
+        if i % 3 == 0:
+            steps = steps * 1024.0                                # far below: exp underflows
+        r = torch.clamp(x0 - steps * spacing, min=-torch.finfo(dt).max).to(dt)
+        m = 1 + i % 4
+        pos = torch.randperm(E, generator=g)[:m]
+        r[pos] = x0.to(dt)
+        rows.append(r)
+    l = torch.stack(rows)
+    assert torch.isfinite(l.float()).all()
+    idx, w = moe.moe_route(l.to(DEV), k, renorm)
+    torch.cuda.synchronize()
+    arr, name = storage(l)
+    ridx, rw = O.route(O.to_f64(arr, name), k, renorm, name)
+    np.testing.assert_array_equal(u32(idx), ridx)
+    check_weights(w, rw, f"large logits {name} E={E} k={k}")
+
+
 @pytest.mark.parametrize("renorm", [True, False])
 def test_route_sweep_full_size(renorm):
     """The routing-only workload at full size: [1 048 576, 64] bf16, N(0, 2^2), top_k = 8."""
