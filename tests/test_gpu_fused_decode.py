@@ -128,3 +128,40 @@ def test_fused_sigmoid_forward_equals_stages(name, T, E, k, H, I, G, SG, top2):
     ref = O.forward_rows(xs, ridx[tok], rw[tok],
                          oracle_expert_weights(g["gate"], g["up"], g["down"], "bf16"))
     assert rel_max_err(f64(out)[tok], ref) <= layer_tol(torch.bfloat16)
+
+
+PAIR_CASES = [
+    # name, T, E, k, H, I, dtype, zipf: experts average >= 128 rows, so the layer takes the CTA-pair
+    # kernels (256-row tiles, 128-row tails)
+    ("bf16_e4", 600, 4, 2, 256, 192, "bf16", 1.0),
+    ("f16_e16_ragged", 2000, 16, 2, 512, 256, "f16", 1.3),
+    ("bf16_e8_k3_steep", 1003, 8, 3, 128, 384, "bf16", 2.0),
+]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=[c[0] for c in PAIR_CASES])
+def test_forward_pair_equals_stages(case):
+    """moe_forward on the CTA-pair path equals, bit for bit, the stage calls (route, dispatch,
+    experts on x_d, combine) on ragged experts, and a sample of tokens matches the oracle."""
+    name, T, E, k, H, I, dt, zipf = case
+    assert not moe.moe_forward_fused(T, E, H, I, k, TORCH_DT[dt], TORCH_DT[dt])
+    wl = W.Workload(name, T=T, E=E, top_k=k, renormalize=True, dtype=dt, seed=41, H=H, I=I,
+                    zipf_s=zipf)
+    g = W.make_layer_inputs(wl, DEV)
+    out = moe.moe_forward(g["x"], g["logits"], g["gate"], g["up"], g["down"], k, True)
+    idx, w = moe.moe_route(g["logits"], k, True)
+    d = moe.moe_dispatch(g["x"], idx, E)
+    y = moe.moe_experts_forward_dispatched(d["x_d"], d["offsets"], g["gate"], g["up"], g["down"])
+    staged = moe.moe_combine(y, d["row_of_slot"], w)
+    torch.cuda.synchronize()
+    counts = np.diff(d["offsets"].cpu().numpy())
+    assert counts.max() > 256, counts     # several 256-row tiles in one expert
+    if name != "bf16_e4":                 # and experts whose last tile has <= 128 rows
+        assert ((counts % 256 > 0) & (counts % 256 <= 128)).any(), counts
+    assert torch.equal(out.view(torch.uint8), staged.view(torch.uint8)), "forward != stages"
+    larr, lname = storage(g["logits"])
+    ridx, rw = O.route(O.to_f64(larr, lname), k, True, lname)
+    tok = np.sort(np.random.default_rng(2).choice(T, 24, replace=False))
+    xs = O.to_f64(storage(g["x"][torch.from_numpy(tok).to(DEV)])[0], dt)
+    ref = O.forward_rows(xs, ridx[tok], rw[tok], oracle_expert_weights(g["gate"], g["up"], g["down"], dt))
+    assert rel_max_err(f64(out)[tok], ref) <= layer_tol(g["x"].dtype)
