@@ -131,15 +131,6 @@ __device__ __forceinline__ float exp_nonpos(float d) {
   const float h = ex2_ftz(d * (0.5f * kLog2e));
   return h * h;
 }
-// the storage bits of a 16-bit value
-template <typename T>
-__device__ __forceinline__ uint32_t bits16(T v) {
-  if constexpr (Dt<T>::code == MOE_BF16) {
-    return __bfloat16_as_ushort(v);
-  } else {
-    return __half_as_ushort(v);
-  }
-}
 
 // Weights of the chosen experts (ids, logits) and the stores of one row.
 template <typename T, bool RENORM>
@@ -164,10 +155,17 @@ __device__ __forceinline__ void emit_row(uint32_t (&id)[8], const float (&x)[8],
     uint4* io = reinterpret_cast<uint4*>(idx_out + row * 8);
     io[0] = make_uint4(id[0], id[1], id[2], id[3]);
     io[1] = make_uint4(id[4], id[5], id[6], id[7]);
-    uint32_t p[4];
+    uint32_t p[4];  // two weights per word, each rounded to nearest even, the first in the low half
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      p[j] = bits16<T>(Dt<T>::from_f(wt[2 * j])) | (bits16<T>(Dt<T>::from_f(wt[2 * j + 1])) << 16);
+    for (int j = 0; j < 4; ++j) {
+      if constexpr (Dt<T>::code == MOE_BF16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(wt[2 * j], wt[2 * j + 1]);
+        p[j] = *reinterpret_cast<const uint32_t*>(&h);
+      } else {
+        const __half2 h = __floats2half2_rn(wt[2 * j], wt[2 * j + 1]);
+        p[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+    }
     *reinterpret_cast<uint4*>(w_out + row * 8) = make_uint4(p[0], p[1], p[2], p[3]);
   } else {
     uint32_t* io = idx_out + row * k;
