@@ -132,19 +132,54 @@ __device__ __forceinline__ float exp_nonpos(float d) {
   return h * h;
 }
 
+// Softmax denominator of one row over all E experts against its maximum x0: sum of exp(x - x0)
+// = 2^((x - x0) log2 e), read again from the row's vectors (rowv[v ^ sw]).  Terms below 2^-126
+// are flushed to zero, which leaves the sum (>= 1, the maximum's own term) unchanged.  For
+// |x0| <= 64 the exponent is one FFMA, x log2 e - x0 log2 e, whose rounding of x0 log2 e costs at
+// most 2^-24 * 93 < 6e-6 in the exponent; larger maxima subtract first.
+template <typename T, int NV>
+__device__ __forceinline__ float row_denominator(const uint4* rowv, int sw, float x0) {
+  float s0 = 0.f, s1 = 0.f;
+  if (fabsf(x0) <= 64.f) {
+    const float c = x0 * kLog2e;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const uint4 q = rowv[v ^ sw];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s0 += ex2_ftz(fmaf(bits16_to_float<T>(w[i] & 0xFFFFu), kLog2e, -c));
+        s1 += ex2_ftz(fmaf(bits16_to_float<T>(w[i] >> 16), kLog2e, -c));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const uint4 q = rowv[v ^ sw];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        s0 += ex2_ftz((bits16_to_float<T>(w[i] & 0xFFFFu) - x0) * kLog2e);
+        s1 += ex2_ftz((bits16_to_float<T>(w[i] >> 16) - x0) * kLog2e);
+      }
+    }
+  }
+  return s0 + s1;
+}
+
 // Weights of the chosen experts (ids, logits) and the stores of one row.
-template <typename T, bool RENORM>
+template <typename T, int NV, bool RENORM>
 __device__ __forceinline__ void emit_row(uint32_t (&id)[8], const float (&x)[8], bool poisoned,
-                                         float x0, float sum, int k, int vec_store,
-                                         uint32_t* __restrict__ idx_out, T* __restrict__ w_out,
-                                         int64_t row) {
+                                         float x0, const uint4* rowv, int sw, int k,
+                                         int vec_store, uint32_t* __restrict__ idx_out,
+                                         T* __restrict__ w_out, int64_t row) {
   float ex[8], sel = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     ex[j] = exp_nonpos(x[j] - x0);
     if (j < k) sel += ex[j];
   }
-  const float inv = 1.f / (RENORM ? sel : sum);
+  const float inv = 1.f / (RENORM || poisoned ? sel : row_denominator<T, NV>(rowv, sw, x0));
   float wt[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -185,7 +220,7 @@ __device__ __forceinline__ void emit_row(uint32_t (&id)[8], const float (&x)[8],
 // is a zero or tiny (for those it is called out of line, so that the common path holds no
 // registers for it).  Vector v of the row is rowv[v ^ sw] (shared or global memory).
 template <typename T, int NV, bool RENORM>
-__device__ __forceinline__ void exact_row(const uint4* rowv, int sw, float x0, float sum, int k,
+__device__ __forceinline__ void exact_row(const uint4* rowv, int sw, float x0, int k,
                                           int vec_store, uint32_t* idx_out, T* w_out,
                                           int64_t row) {
   uint32_t top[8];
@@ -221,17 +256,17 @@ __device__ __forceinline__ void exact_row(const uint4* rowv, int sw, float x0, f
     id[j] = 0xFFFFu - (top[j] & 0xFFFFu);
     x[j] = bits16_to_float<T>((t & 0x8000u) ? (t & 0x7FFFu) : (~t & 0xFFFFu));
   }
-  emit_row<T, RENORM>(id, x, false, x0, sum, k, vec_store, idx_out, w_out, row);
+  emit_row<T, NV, RENORM>(id, x, false, x0, rowv, sw, k, vec_store, idx_out, w_out, row);
 }
 template <typename T, int NV, bool RENORM>
-__device__ __noinline__ void exact_row_outlined(const uint4* rowv, int sw, float x0, float sum,
-                                                int k, int vec_store, uint32_t* idx_out,
-                                                T* w_out, int64_t row) {
-  exact_row<T, NV, RENORM>(rowv, sw, x0, sum, k, vec_store, idx_out, w_out, row);
+__device__ __noinline__ void exact_row_outlined(const uint4* rowv, int sw, float x0, int k,
+                                                int vec_store, uint32_t* idx_out, T* w_out,
+                                                int64_t row) {
+  exact_row<T, NV, RENORM>(rowv, sw, x0, k, vec_store, idx_out, w_out, row);
 }
 
 template <typename T, int NV, bool RENORM>
-__global__ void __launch_bounds__(256, RENORM ? 5 : 4)
+__global__ void __launch_bounds__(256, (RENORM || Dt<T>::code == MOE_BF16) ? 5 : 4)
     moe_route16_small(const uint4* __restrict__ logits, int64_t T_, int k, int vec_store,
                       uint32_t* __restrict__ idx_out, T* __restrict__ w_out) {
   constexpr uint32_t EXPMASK = Dt<T>::code == MOE_BF16 ? 0x7F80u : 0x7C00u;
@@ -284,34 +319,21 @@ __global__ void __launch_bounds__(256, RENORM ? 5 : 4)
   const bool pos = mb >= 1023u && mb < 0x8000u;          // positive maximum, window all >= 0
   const bool neg = mb > 0x8000u && mb <= 0xFC00u;        // negative maximum, so is every value
   const float x0 = bits16_to_float<T>(mb);
-  float sum = 0.f;
-  if (!RENORM) {
-    // softmax denominator over all experts against the row maximum, exp(x - x0) = 2^((x - x0)
-    // log2 e).  Terms below 2^-126 are flushed to zero, which leaves the sum (>= 1, the maximum's
-    // own term) unchanged.
-    float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-    for (int j = 0; j < NV * 4; ++j) {
-      s0 += ex2_ftz((bits16_to_float<T>(wv[j] & 0xFFFFu) - x0) * kLog2e);
-      s1 += ex2_ftz((bits16_to_float<T>(wv[j] >> 16) - x0) * kLog2e);
-    }
-    sum = s0 + s1;
-  }
 
   const uint4* rowv = STAGED ? tile + tid * 8 : src;
   const int sw = STAGED ? (tid & 7) : 0;
   if (poisoned) {
     uint32_t id[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     const float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    emit_row<T, RENORM>(id, x, true, x0, sum, k, vec_store, idx_out, w_out, row);
+    emit_row<T, NV, RENORM>(id, x, true, x0, rowv, sw, k, vec_store, idx_out, w_out, row);
     return;
   }
   if constexpr (!HALF) {
-    exact_row<T, NV, RENORM>(rowv, sw, x0, sum, k, vec_store, idx_out, w_out, row);
+    exact_row<T, NV, RENORM>(rowv, sw, x0, k, vec_store, idx_out, w_out, row);
     return;
   }
   if (!(pos || neg)) {
-    exact_row_outlined<T, NV, RENORM>(rowv, sw, x0, sum, k, vec_store, idx_out, w_out, row);
+    exact_row_outlined<T, NV, RENORM>(rowv, sw, x0, k, vec_store, idx_out, w_out, row);
     return;
   }
 
@@ -350,7 +372,7 @@ __global__ void __launch_bounds__(256, RENORM ? 5 : 4)
     clean8<true>(top);
   }
   if ((top[7] & 0xFFFFu) >= 1023u * 64u) {  // the 8th key squashed: decide again exactly
-    exact_row_outlined<T, NV, RENORM>(rowv, sw, x0, sum, k, vec_store, idx_out, w_out, row);
+    exact_row_outlined<T, NV, RENORM>(rowv, sw, x0, k, vec_store, idx_out, w_out, row);
     return;
   }
   // chosen ids, and their logits: bf16 bits ((mf - d) ^ flip) << 16 = (mf << 16) - (d << 16)
@@ -363,7 +385,7 @@ __global__ void __launch_bounds__(256, RENORM ? 5 : 4)
     id[j] = top[j] & 63u;
     x[j] = __uint_as_float((m16 - (top[j] & 0xFFC0u) * 1024u) ^ fl16);
   }
-  emit_row<T, RENORM>(id, x, false, x0, sum, k, vec_store, idx_out, w_out, row);
+  emit_row<T, NV, RENORM>(id, x, false, x0, rowv, sw, k, vec_store, idx_out, w_out, row);
 }
 
 template <typename T>
