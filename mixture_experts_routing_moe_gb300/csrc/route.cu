@@ -125,46 +125,58 @@ __device__ __forceinline__ float ex2_ftz(float y) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
   return r;
 }
-// exp(d) for d <= 0 as (2^(d log2 e / 2))^2: the half power stays normal down to d log2 e = -252,
-// and the square (an IEEE multiply) rounds into the subnormal range where the result lies there
-__device__ __forceinline__ float exp_nonpos(float d) {
-  const float h = ex2_ftz(d * (0.5f * kLog2e));
-  return h * h;
+
+// Two FP32 lanes in one 64-bit register, low lane first, and the packed FP32 operations of
+// sm_100 and later (one instruction for both lanes, each lane rounded as its scalar form).
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
 }
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
 
 // Softmax denominator of one row over all E experts against its maximum x0: sum of exp(x - x0)
-// = 2^((x - x0) log2 e), read again from the row's vectors (rowv[v ^ sw]).  Terms below 2^-126
-// are flushed to zero, which leaves the sum (>= 1, the maximum's own term) unchanged.  For
-// |x0| <= 64 the exponent is one FFMA, x log2 e - x0 log2 e, whose rounding of x0 log2 e costs at
-// most 2^-24 * 93 < 6e-6 in the exponent; larger maxima subtract first.
-template <typename T, int NV>
-__device__ __forceinline__ float row_denominator(const uint4* rowv, int sw, float x0) {
-  float s0 = 0.f, s1 = 0.f;
-  if (fabsf(x0) <= 64.f) {
-    const float c = x0 * kLog2e;
+// = 2^((x - x0) log2 e), read again from the row's vectors (rowv[v ^ sw]), both logits of a
+// 32-bit word in the two lanes of packed FP32 operations.  Terms below 2^-126 are flushed to
+// zero, which leaves the sum (>= 1, the maximum's own term) unchanged.  For |x0| <= 64 the
+// exponent is one FMA, x log2 e - x0 log2 e, whose rounding of x0 log2 e costs at most
+// 2^-24 * 93 < 6e-6 in the exponent; larger maxima subtract first.
+template <typename T, int NV, bool SMALL>
+__device__ __forceinline__ float row_denominator_t(const uint4* rowv, int sw, float x0) {
+  const uint64_t l2 = f32x2(kLog2e, kLog2e);
+  const uint64_t c2 = SMALL ? f32x2(-x0 * kLog2e, -x0 * kLog2e) : f32x2(-x0, -x0);
+  uint64_t acc = 0ull;
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      const uint4 q = rowv[v ^ sw];
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  for (int v = 0; v < NV; ++v) {
+    const uint4 q = rowv[v ^ sw];
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        s0 += ex2_ftz(fmaf(bits16_to_float<T>(w[i] & 0xFFFFu), kLog2e, -c));
-        s1 += ex2_ftz(fmaf(bits16_to_float<T>(w[i] >> 16), kLog2e, -c));
-      }
-    }
-  } else {
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      const uint4 q = rowv[v ^ sw];
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        s0 += ex2_ftz((bits16_to_float<T>(w[i] & 0xFFFFu) - x0) * kLog2e);
-        s1 += ex2_ftz((bits16_to_float<T>(w[i] >> 16) - x0) * kLog2e);
-      }
+    for (int i = 0; i < 4; ++i) {
+      const uint64_t x = f32x2(bits16_to_float<T>(w[i] & 0xFFFFu), bits16_to_float<T>(w[i] >> 16));
+      const uint64_t y = SMALL ? fma_f32x2(x, l2, c2) : mul_f32x2(add_f32x2(x, c2), l2);
+      acc = add_f32x2(acc, f32x2(ex2_ftz(lo_f32(y)), ex2_ftz(hi_f32(y))));
     }
   }
-  return s0 + s1;
+  return lo_f32(acc) + hi_f32(acc);
+}
+template <typename T, int NV>
+__device__ __forceinline__ float row_denominator(const uint4* rowv, int sw, float x0) {
+  return fabsf(x0) <= 64.f ? row_denominator_t<T, NV, true>(rowv, sw, x0)
+                           : row_denominator_t<T, NV, false>(rowv, sw, x0);
 }
 
 // Weights of the chosen experts (ids, logits) and the stores of one row.
@@ -173,19 +185,31 @@ __device__ __forceinline__ void emit_row(uint32_t (&id)[8], const float (&x)[8],
                                          float x0, const uint4* rowv, int sw, int k,
                                          int vec_store, uint32_t* __restrict__ idx_out,
                                          T* __restrict__ w_out, int64_t row) {
-  float ex[8], sel = 0.f;
+  // exp(x - x0) of the chosen logits as (2^((x - x0) log2 e / 2))^2, two per packed operation:
+  // the half power stays normal down to (x - x0) log2 e = -252, and the square (an IEEE multiply)
+  // rounds into the subnormal range where the result lies there
+  uint64_t ex[4];
+  float sel = 0.f;
+  const uint64_t nx0 = f32x2(-x0, -x0), hl2 = f32x2(0.5f * kLog2e, 0.5f * kLog2e);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    ex[j] = exp_nonpos(x[j] - x0);
-    if (j < k) sel += ex[j];
+  for (int j = 0; j < 4; ++j) {
+    const uint64_t y = mul_f32x2(add_f32x2(f32x2(x[2 * j], x[2 * j + 1]), nx0), hl2);
+    const uint64_t h = f32x2(ex2_ftz(lo_f32(y)), ex2_ftz(hi_f32(y)));
+    ex[j] = mul_f32x2(h, h);
+    if (2 * j < k) sel += lo_f32(ex[j]);
+    if (2 * j + 1 < k) sel += hi_f32(ex[j]);
   }
   const float inv = 1.f / (RENORM || poisoned ? sel : row_denominator<T, NV>(rowv, sw, x0));
   float wt[8];
+  const uint64_t inv2 = f32x2(inv, inv);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    id[j] = poisoned ? (uint32_t)j : id[j];
-    wt[j] = poisoned ? __int_as_float(0x7FC00000) : ex[j] * inv;
+  for (int j = 0; j < 4; ++j) {
+    const uint64_t q = mul_f32x2(ex[j], inv2);
+    wt[2 * j] = poisoned ? __int_as_float(0x7FC00000) : lo_f32(q);
+    wt[2 * j + 1] = poisoned ? __int_as_float(0x7FC00000) : hi_f32(q);
   }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) id[j] = poisoned ? (uint32_t)j : id[j];
   if (vec_store) {  // k == 8, 16-byte aligned outputs
     uint4* io = reinterpret_cast<uint4*>(idx_out + row * 8);
     io[0] = make_uint4(id[0], id[1], id[2], id[3]);
