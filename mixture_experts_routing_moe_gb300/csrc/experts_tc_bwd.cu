@@ -357,10 +357,15 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
           break;
         }
         const uint32_t sa = base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+        int nkk = BK / 16;  // K = 16 steps of this stage that hold the expert's rows
         if (MODE == WG) {
           const int valid = r1 - (r0 + kb * BK);
-          if (valid < BK) {  // rows past the expert's end belong to the next expert: zero them
-            const int nz = (BK - valid) * 6 * 8;  // rows x (2 A + 4 B boxes) x 8 chunks
+          if (valid < BK) {
+            // the last stage of an expert: only ceil(valid / 16) K steps are issued, and the rows
+            // between the expert's end and that step's end (they belong to the next expert) are
+            // zeroed in both operands
+            nkk = (valid + 15) / 16;
+            const int nz = (nkk * 16 - valid) * 6 * 8;  // rows x (2 A + 4 B boxes) x 8 chunks
             uint8_t* g0 = gbase + stage * STAGE_BYTES;
             for (int i = lane; i < nz; i += 32) {
               const int row = valid + i / 48, rem = i % 48, box = rem / 8, ch = rem % 8;
@@ -378,8 +383,9 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
           const uint64_t db = B_MN ? make_sdesc_mn(sb) : make_sdesc(sb);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)  // 16 K: 32 bytes (K-major) or 2 KB (MN-major)
-            umma_f16(d_tmem, da + (A_MN ? 128u : 2u) * kk, db + (B_MN ? 128u : 2u) * kk, idesc,
-                     (kb | kk) != 0);
+            if (kk < nkk)
+              umma_f16(d_tmem, da + (A_MN ? 128u : 2u) * kk, db + (B_MN ? 128u : 2u) * kk, idesc,
+                       (kb | kk) != 0);
           umma_commit_mc(empty_bar(stage), 0x3);  // frees the stage in both CTAs
         }
         __syncwarp();
