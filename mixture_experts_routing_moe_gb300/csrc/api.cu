@@ -31,10 +31,10 @@ struct Cursor {
 struct FwdLayout {
   size_t idx, w, ros, tor, offsets, hist, ready, xd, a, total;
 };
-// counters of the fused short-batch launch: per m-tile (gate/up stored), then per (m-tile,
-// down n-tile) (y stored)
+// counters of the fused short-batch launch: per m-tile (gate/up stored), per (m-tile, down
+// n-tile) (y stored), per m-tile (x_d rows gathered), then one flag (row_of_slot written)
 size_t ready_bytes(int64_t R, int64_t E, int64_t H) {
-  return (size_t)((R + 127) / 128 + E + 1) * (size_t)(1 + (H + 255) / 256) * 4;
+  return ((size_t)((R + 127) / 128 + E + 1) * (size_t)(2 + (H + 255) / 256) + 1) * 4;
 }
 
 FwdLayout fwd_layout(int64_t T, int64_t E, int64_t H, int64_t I, int k, int ldt, int wdt) {

@@ -6,13 +6,17 @@
 // microseconds between grid barriers.
 //
 // One CTA per SM (cooperative launch, so all CTAs are resident and may wait on each other), the
-// warp roles of the single-CTA expert GEMM (gemm_cta.cuh), phases separated by grid barriers:
+// warp roles of the single-CTA expert GEMM (gemm_cta.cuh); one grid barrier, after the route,
+// and counters in global memory for every later hand-over between CTAs:
 //   1. route     token rows strided over all warps of the grid; one warp per row, the same
 //                arithmetic as the route kernel (route_core.cuh) -> idx, w in the workspace.
 //   2. dispatch  every CTA sorts all T * k slots in shared memory (dispatch_core.cuh; the same
-//                stable order as the dispatch kernels); CTA 0 publishes offsets and row_of_slot;
-//                each CTA gathers its contiguous share of the rows of x_d.
-//   3. gate/up   the single-CTA tcgen05 GEMM over the tile list of the offsets -> a.
+//                stable order as the dispatch kernels); CTA 0 publishes offsets and row_of_slot
+//                (then raises a flag the combine waits for); each CTA gathers its contiguous
+//                share of the rows of x_d and adds the rows it copied to a per-m-tile count.
+//   3. gate/up   the single-CTA tcgen05 GEMM over the tile list of the offsets -> a; a tile's
+//                producer loads B at once and A once the m-tile's gathered count equals its
+//                rows.  Every CTA finishes its gather before its first tile, so every wait ends.
 //   4. down      the same GEMM on a -> y (y reuses the x_d buffer).  No barrier before it: a
 //                per-m-tile count of stored gate/up warps gates the A loads of each down tile,
 //                so the down GEMM starts while the last gate/up tiles are still running.
@@ -20,9 +24,9 @@
 //                waiting only for the down tiles it reads (no grid barrier before it).
 // Data written in one phase and read in a later one goes through L2 only: generic loads use
 // ld.global.cg, and x_d / a, which the next phase reads with TMA, are ordered for the async proxy
-// by fence.proxy.async on both sides of the barrier.  Every wait (mbarriers and the grid barrier)
-// is bounded; on expiry the status word gets the timeout bit, later phases are skipped and the
-// kernel still releases TMEM and exits.
+// by fence.proxy.async on both sides of the count that hands them over.  Every wait (mbarriers,
+// the grid barrier and the counts) is bounded; on expiry the status word gets the timeout bit,
+// later phases are skipped and the kernel still releases TMEM and exits.
 #include <cuda.h>
 
 #include <type_traits>
@@ -77,7 +81,8 @@ struct DecodeParams {
   unsigned* grid_count;   // zero at launch
   unsigned* tile_count;   // zeroed in phase 1: GEMM tiles claimed after the static first ones
   unsigned* mtile_ready;  // [n_ready], zeroed in phase 1: stored gate/up warps per m-tile
-                          // [n_mtiles], then stored down warps per (m-tile, n-tile)
+                          // [n_mtiles], stored down warps per (m-tile, n-tile), gathered x_d
+                          // rows per m-tile [n_mtiles], then the row_of_slot flag
   int n_ready, n_mtiles;
   TcParams gu, dn;        // offsets filled in by the kernel (shared memory)
 };
@@ -135,6 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* scratch = fd_smem_raw + (ring.base - smem_u32(fd_smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t R = (int64_t)p.T * p.k;
+  // x_d rows gathered per m-tile, then the row_of_slot flag (after the per-(m-tile, n-tile) y
+  // counts of the down epilogue)
+  unsigned* gathered = p.mtile_ready + (size_t)p.n_mtiles * (1 + p.dn.NT);
+  unsigned* ros_flag = gathered + p.n_mtiles;
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < kTileSlots; ++q) {
@@ -160,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   EpilogueState est;
 
   // ---------------------------------------------------------------- 1. route
-  if (blockIdx.x == 0) {  // counters first used after barrier 2: zeroed here, not by the host
+  if (blockIdx.x == 0) {  // counters first used after the grid barrier: zeroed here, not by the host
     if (threadIdx.x == 0) *p.tile_count = 0u;
     for (int i = threadIdx.x; i < p.n_ready; i += blockDim.x) p.mtile_ready[i] = 0u;
   }
@@ -231,6 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     dispatch_scatter<true>(idx_s, R, p.E, p.k, CH, hist, tor, lead ? p.row_of_slot : nullptr);
     __syncthreads();
+    if (lead && threadIdx.x == 0) {  // row_of_slot is complete: the combine waits for this flag
+      __threadfence();
+      atomicAdd(ros_flag, 1u);
+    }
     // rows [r0, r1) of x_d: x_d[r] = x[token_of_row[r]], 16-byte vectors
     // 32-bit index arithmetic: R <= 4096 rows of H / 8 <= 2^16 vectors (64-bit division is slow)
     const uint32_t per = (uint32_t)((R + gridDim.x - 1) / gridDim.x);
@@ -256,10 +269,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int b = 0; b < kInFlight; ++b)
         if (i0 + b * blockDim.x < nvec) st_v4(xd + dst[b], v[b]);
     }
-    // x_d is read by TMA after the barrier, and TMA refills this scratch shared memory
+    // x_d is read by TMA (other CTAs' gate/up producers), and TMA refills this scratch shared
+    // memory: generic writes made visible to the async proxy, then the rows are counted per
+    // m-tile (a producer loads an m-tile's A rows once its count equals its rows)
     fence_proxy_async_all();
+    __syncthreads();
+    if (threadIdx.x == 0 && r0 < r1) {
+      __threadfence();
+      for (uint32_t r = r0; r < r1;) {
+        const int e = find_expert(offs, p.E, (int)r);  // offs[e] <= r < offs[e + 1]
+        const int m = ((int)r - offs[e]) / BM;
+        const uint32_t end = min(r1, (uint32_t)min(offs[e + 1], offs[e] + (m + 1) * BM));
+        atomicAdd(gathered + pref[e] + m, end - r);
+        r = end;
+      }
+    }
   }
-  grid_barrier(p.grid_count, 2, ring.abort_f, p.status);
+  __syncthreads();
 
   // ---------------------------------------------------------------- 3. gate/up, 4. down
   // One tile list: the gate/up tiles, then the down tiles, claimed dynamically (a global counter)
@@ -271,6 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     TcParams gu = p.gu, dn = p.dn;
     gu.offsets = offs;
     dn.offsets = offs;
+    gu.ready_wait = gathered;  // target 0: the rows of the m-tile
+    gu.ready_target = 0u;
     gu.ready_signal = p.mtile_ready;
     dn.ready_wait = p.mtile_ready;
     dn.ready_target = 4u * (unsigned)gu.NT;
@@ -345,7 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t chunks = (int64_t)p.H * 2 / 16;
     const int64_t wpt = (chunks + 31) / 32;  // = the down GEMM's n-tiles (256 columns each)
     const unsigned* y_ready = p.mtile_ready + p.n_mtiles;
-    for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < (int64_t)p.T * wpt;
+    int ros_ok = 1;
+    if (lane == 0) ros_ok = wait_count(ros_flag, 1u, ring.abort_f, p.status);
+    ros_ok = __shfl_sync(0xFFFFFFFFu, ros_ok, 0);
+    for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; ros_ok && it < (int64_t)p.T * wpt;
          it += (int64_t)gridDim.x * kWarps) {
       const int64_t t = (uint32_t)it / (uint32_t)wpt;  // 32-bit division (it < T * wpt)
       const int c = (int)(it - t * wpt);
@@ -429,7 +460,7 @@ cudaError_t launch_t(const FusedDecodeArgs& f, cudaStream_t s) {
   p.tile_count = f.tile_count;
   p.mtile_ready = f.mtile_ready;
   p.n_mtiles = (int)((R + BM - 1) / BM + f.E + 1);
-  p.n_ready = p.n_mtiles * (1 + (f.H + BN - 1) / BN);
+  p.n_ready = p.n_mtiles * (2 + (f.H + BN - 1) / BN) + 1;
   p.gu.out = (uint8_t*)f.a;
   p.gu.status = f.status;
   p.gu.E = f.E;

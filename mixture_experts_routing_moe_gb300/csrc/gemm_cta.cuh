@@ -77,7 +77,8 @@ struct TcParams {
   // Dataflow between two GEMMs of one launch (null when unused).  ready_signal: the epilogue
   // adds 1 per warp to ready_signal[global m-tile] once its rows of a tile are stored.
   // ready_wait: before the first A load of a tile the producer waits until
-  // ready_wait[global m-tile] >= ready_target.  Global m-tile = pref[e] + m.
+  // ready_wait[global m-tile] >= ready_target (0: the number of rows of that m-tile).  Global
+  // m-tile = pref[e] + m.
   unsigned* ready_signal;
   const unsigned* ready_wait;
   unsigned ready_target;
@@ -204,9 +205,13 @@ __device__ __forceinline__ bool producer_tile(const CUtensorMap* mapA, const CUt
     } else {
       tma_load_2d(sb, mapB0, r.full_bar(st.stage), kb * BK, b_row, pb);
     }
-    if (kb == 0 && p.ready_wait &&
-        !wait_count(p.ready_wait + pref[e] + m, p.ready_target, r.abort_f, p.status))
-      return false;
+    if (kb == 0 && p.ready_wait) {
+      // ready_target 0: wait for one count per row of the m-tile
+      const unsigned target =
+          p.ready_target ? p.ready_target
+                         : (unsigned)min(BM, off_at<FUSED>(p.offsets, e + 1) - a_row);
+      if (!wait_count(p.ready_wait + pref[e] + m, target, r.abort_f, p.status)) return false;
+    }
     tma_load_2d(sa, mapA, r.full_bar(st.stage), kb * BK, a_row, pa);
     if (++st.stage == STAGES) {
       st.stage = 0;
