@@ -117,7 +117,7 @@ __device__ __forceinline__ bool sigmoid_row_fp32(const T* __restrict__ src,
       if (g < 64 ? (chosen_lo >> g) & 1ull : (chosen_hi >> (g - 64)) & 1ull) avail |= 1u << i;
     }
   }
-  float prev = 0.f, my_c = 0.f;
+  float prev = 0.f;
   int my_id = -1;
   for (int r = 0; r < k + (k < cand ? 1 : 0); ++r) {
     float bv = -INFINITY;
