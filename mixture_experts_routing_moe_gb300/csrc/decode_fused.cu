@@ -10,10 +10,13 @@
 // and counters in global memory for every later hand-over between CTAs:
 //   1. route     token rows strided over all warps of the grid; one warp per row, the same
 //                arithmetic as the route kernel (route_core.cuh) -> idx, w in the workspace.
-//   2. dispatch  every CTA sorts all T * k slots in shared memory (dispatch_core.cuh; the same
-//                stable order as the dispatch kernels); CTA 0 publishes offsets and row_of_slot
-//                (then raises a flag the combine waits for); each CTA gathers its contiguous
-//                share of the rows of x_d and adds the rows it copied to a per-m-tile count.
+//   2. dispatch  every CTA counts all T * k slots in shared memory (dispatch_core.cuh: the
+//                offsets and, per warp chunk, each expert's first row; CTA 0 publishes the
+//                offsets); each CTA takes a contiguous share of the rows of x_d, finds each row's
+//                slot in the stable order (ascending slot order inside an expert, as in the
+//                dispatch kernels), writes its row_of_slot entry, gathers the row, and adds the
+//                rows it copied to a per-m-tile count and to a row_of_slot count the combine
+//                waits for.
 //   3. gate/up   the single-CTA tcgen05 GEMM over the tile list of the offsets -> a; a tile's
 //                producer loads B at once and A once the m-tile's gathered count equals its
 //                rows.  Every CTA finishes its gather before its first tile, so every wait ends.
@@ -140,10 +143,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* scratch = fd_smem_raw + (ring.base - smem_u32(fd_smem_raw));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t R = (int64_t)p.T * p.k;
-  // x_d rows gathered per m-tile, then the row_of_slot flag (after the per-(m-tile, n-tile) y
-  // counts of the down epilogue)
+  // x_d rows gathered per m-tile, then the row_of_slot entries written (after the per-(m-tile,
+  // n-tile) y counts of the down epilogue)
   unsigned* gathered = p.mtile_ready + (size_t)p.n_mtiles * (1 + p.dn.NT);
-  unsigned* ros_flag = gathered + p.n_mtiles;
+  unsigned* ros_count = gathered + p.n_mtiles;
 
   if (threadIdx.x == 0) {
     for (int q = 0; q < kTileSlots; ++q) {
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     const int CH = (int)(((R + kWarps - 1) / kWarps + 31) / 32 * 32);
-    const bool lead = blockIdx.x == 0;
+    const bool lead = blockIdx.x == 0;  // publishes the offsets
     dispatch_count<true>(idx_s, R, p.E, kWarps, CH, hist, off_s, lead ? p.offsets : nullptr,
                          lead ? p.status : nullptr);
     for (int e = threadIdx.x; e <= p.E; e += blockDim.x) offs[e] = off_s[e];
@@ -238,16 +241,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.up) + row0 * p.H * 2, bytes);
       }
     }
-    dispatch_scatter<true>(idx_s, R, p.E, p.k, CH, hist, tor, lead ? p.row_of_slot : nullptr);
-    __syncthreads();
-    if (lead && threadIdx.x == 0) {  // row_of_slot is complete: the combine waits for this flag
-      __threadfence();
-      atomicAdd(ros_flag, 1u);
-    }
-    // rows [r0, r1) of x_d: x_d[r] = x[token_of_row[r]], 16-byte vectors
+    // Rows [r0, r1) of x_d are this CTA's.  Their slots come straight from the sorted order
+    // instead of a full scatter: after dispatch_count, hist[c * E + e] is the first row of
+    // expert e among the slots of chunk c, so row r of expert e is the (r - hist[c * E + e])-th
+    // slot holding e in the last chunk c whose first row is <= r.  Every row is gathered by
+    // exactly one CTA, which also writes its slot's row_of_slot entry.
     // 32-bit index arithmetic: R <= 4096 rows of H / 8 <= 2^16 vectors (64-bit division is slow)
     const uint32_t per = (uint32_t)((R + gridDim.x - 1) / gridDim.x);
     const uint32_t r0 = min((uint32_t)R, blockIdx.x * per), r1 = min((uint32_t)R, r0 + per);
+    for (uint32_t r = r0 + warp; r < r1; r += kWarps) {
+      const int e = find_expert(offs, p.E, (int)r);  // offs[e] <= r < offs[e + 1]
+      int c = 0;
+      for (int cc = 1; cc < kWarps; ++cc)
+        if (hist[cc * p.E + e] <= (int)r) c = cc;
+      int q = (int)r - hist[c * p.E + e];
+      const uint32_t cend = (uint32_t)min(R, (int64_t)(c + 1) * CH);
+      uint32_t slot = 0;
+      for (uint32_t b = (uint32_t)(c * CH); b < cend; b += 32) {
+        const uint32_t sl = b + lane;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, sl < cend && idx_s[sl] == (uint32_t)e);
+        const int n = __popc(m);
+        if (q < n) {  // the (q+1)-th set bit of m
+          slot = b + __fns(m, 0, q + 1);
+          break;
+        }
+        q -= n;
+      }
+      if (lane == 0) {
+        tor[r - r0] = slot / (uint32_t)p.k;
+        p.row_of_slot[slot] = r;
+      }
+    }
+    __syncthreads();
+    // rows [r0, r1) of x_d: x_d[r] = x[token_of_row[r]], 16-byte vectors
     const uint32_t vpr = (uint32_t)p.H / 8;  // 16-byte vectors per row
     const uint4* xs = reinterpret_cast<const uint4*>(p.x);
     uint4* xd = reinterpret_cast<uint4*>(p.x_d);
@@ -262,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i < nvec) {
           const uint32_t rr = i / vpr, c = i - rr * vpr;
           dst[b] = (r0 + rr) * vpr + c;
-          v[b] = ld_nc_v4(xs + (size_t)tor[r0 + rr] * vpr + c);
+          v[b] = ld_nc_v4(xs + (size_t)tor[rr] * vpr + c);
         }
       }
 #pragma unroll
@@ -276,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (threadIdx.x == 0 && r0 < r1) {
       __threadfence();
+      atomicAdd(ros_count, r1 - r0);  // row_of_slot entries written (the combine waits for R)
       for (uint32_t r = r0; r < r1;) {
         const int e = find_expert(offs, p.E, (int)r);  // offs[e] <= r < offs[e + 1]
         const int m = ((int)r - offs[e]) / BM;
@@ -374,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t wpt = (chunks + 31) / 32;  // = the down GEMM's n-tiles (256 columns each)
     const unsigned* y_ready = p.mtile_ready + p.n_mtiles;
     int ros_ok = 1;
-    if (lane == 0) ros_ok = wait_count(ros_flag, 1u, ring.abort_f, p.status);
+    if (lane == 0) ros_ok = wait_count(ros_count, (unsigned)R, ring.abort_f, p.status);
     ros_ok = __shfl_sync(0xFFFFFFFFu, ros_ok, 0);
     for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; ros_ok && it < (int64_t)p.T * wpt;
          it += (int64_t)gridDim.x * kWarps) {
