@@ -43,9 +43,10 @@ def kernels_per_forward(wl) -> int:
     + combine 1."""
     return 1 + (2 if wl.T * wl.top_k <= 4096 else 4) + 2 + 1
 STAGES = ["route", "dispatch", "gate_up_gemm", "down_gemm", "combine"]
-# DRAM traffic of one gate/up GEMM launch on the skewed workload, from the ncu capture summarised
-# in profiles/gateup_tc_skewed.md, valid while experts_tc.cu has the recorded hash.
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gateup_tc_skewed.md")
+# Measured DRAM traffic per launch of the forward GEMM kernels (ncu dram__bytes_read.sum +
+# dram__bytes_write.sum on a small case, scaled to the full workload), recorded together with the
+# hash of the kernel sources it was taken on; used only while the sources still have that hash.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
 
 
 def log(*a):
@@ -64,6 +65,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads measured after the headline one")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward chain (combine, experts, dispatch, router) instead")
     ap.add_argument("--router", choices=["softmax", "sigmoid"], default="softmax",
@@ -220,22 +223,29 @@ def kernel_source_sha256():
     return h.hexdigest()
 
 
-def recorded_traffic():
-    """(bytes per launch, kernel hash) from the committed ncu summary, or None."""
+def recorded_traffic(kernel: str, workload: str):
+    """Bytes per launch of `kernel` on `workload` from the committed traffic record, or None when
+    there is none or the kernel sources have changed since it was taken."""
     try:
-        txt = open(TRAFFIC_FILE).read()
-    except OSError:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    want = {}
-    for line in txt.splitlines():
-        if line.startswith("traffic_bytes_per_full_launch:"):
-            want["bytes"] = float(line.split(":", 1)[1])
-        if line.startswith("kernel_source_sha256:"):
-            want["sha"] = line.split(":", 1)[1].strip()
-    cur = kernel_source_sha256()
-    if "bytes" in want and want.get("sha") == cur:
-        return want["bytes"]
-    return None
+    if rec.get("kernel_source_sha256") != kernel_source_sha256():
+        return None
+    e = rec.get("launches", {}).get(kernel, {}).get(workload)
+    return None if e is None else float(e["bytes_per_launch"])
+
+
+def tensor_peak(pk, clocks, region_s: float):
+    """The bf16 tensor peak a GEMM timed in `region_s` seconds is measured against: the burst
+    figure when the region is shorter than a second and the sampled SM clock stayed at its
+    maximum (the condition the burst GEMM was measured in), else the sustained figure (a
+    seconds-long loop under the power cap)."""
+    at_max = bool(clocks) and clocks["sm_mhz"] >= 0.97 * clocks["sm_max_mhz"]
+    if region_s < 1.0 and at_max:
+        return pk["bf16_tflops"], "burst"
+    return pk["bf16_tflops_sustained"], "sustained"
 
 
 # ------------------------------------------------------------------------------ oracle timing
@@ -338,41 +348,16 @@ def run_route_only(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     wl = W.WORKLOADS[args.workload]
-    logits = W.make_logits(wl, dev)
-    idx = torch.empty(wl.T, wl.top_k, dtype=torch.uint32, device=dev)
-    w = torch.empty(wl.T, wl.top_k, dtype=logits.dtype, device=dev)
-    flush = L2Flush(dev)
-    es = logits.element_size()
-    nbytes = wl.T * wl.E * es + wl.T * wl.top_k * (4 + es)
-    pk, pk_src = peaks()
-    res = {}
-    for renorm in (True, False):
-        for _ in range(max(3, args.warmup)):
-            moe.moe_route(logits, wl.top_k, renorm, idx=idx, w=w)
-        times = []
-        for _ in range(args.steps):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            moe.moe_route(logits, wl.top_k, renorm, idx=idx, w=w)
-            b.record()
-            torch.cuda.synchronize()
-            times.append(a.elapsed_time(b))
-        ms = float(np.mean(times))
-        res["renormalize" if renorm else "plain"] = {"ms": ms, "gbs": nbytes / (ms / 1e3) / 1e9}
+    res, roof, clocks = route_entry(moe, wl, dev, args.steps, args.warmup, L2Flush(dev))
     best = min(res.values(), key=lambda d: d["ms"])
+    roof = {**roof, "achieved": best["gbs"], "frac": best["frac"]}
     line = {"metric": "route GB/s vs HBM (route-only workload)", "value": wl.T / (best["ms"] / 1e3),
             "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": best["ms"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "config": {"workload": f"{wl.name}: logits [{wl.T}, {wl.E}] {wl.dtype}, top_k={wl.top_k}",
                        "l2": "L2 emptied before every launch (256 MB written, then 256 MB read)"},
-            "roofline": {"kernel": ("moe_route16_small" if es == 2 and wl.E <= 64 and wl.E % 8 == 0
-                                    and wl.top_k <= 8 else "moe_route_kernel"), "bound": "hbm",
-                         "achieved": best["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": best["gbs"] / pk["hbm_gbs"], "peak_source": pk_src,
-                         "traffic": None, "algorithmic_bytes_per_launch": nbytes},
-            "variants": res, "gpu_launches": 2 * args.steps}
+            "roofline": roof, "variants": res, "gpu_launches": 2 * args.steps, "clocks": clocks}
     print(json.dumps(line), flush=True)
 
 
@@ -427,10 +412,11 @@ def run_backward(args):
     achieved = flops / (exp_ms / 1e3) / 1e12
     if tensor:
         pk, pk_src = peaks()
-        peak = pk["bf16_tflops_sustained"]
+        peak, kind = tensor_peak(pk, clocks, tot * args.steps / 1e3)
         roof = {"kernel": "experts backward (tcgen05 GEMMs: dA, gate/up + SwiGLU grad, dinput, "
                           "weight grads)", "bound": "tensor",
-                "peak_source": f"{pk_src} bf16 sustained (dense, cuBLAS); f16 runs at the bf16 rate"}
+                "peak_source": f"{pk_src} bf16 {kind} (dense, cuBLAS; chosen from the timed "
+                               f"region's length and sampled clocks); f16 runs at the bf16 rate"}
         launches = 9
     else:
         # FP32 CUDA-core peak from unit counts and clock: SMs x 128 FMA/clk x 2 x max SM clock
@@ -532,27 +518,25 @@ def run_sigmoid(args):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args):
-    import mixture_experts_routing_moe_gb300 as moe
-    from mixture_experts_routing_moe_gb300 import build as build_mod
-    build_mod.build()
-    rank, world, local = dist_setup()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    wl = W.WORKLOADS[args.workload]
+def measure_layer(moe, wl, dev, steps, warmup, world=1, flush=None):
+    """Times `steps` moe_forward calls over one batch of `wl`, inputs resident in HBM.
+
+    Stage times come from CUDA events on the launching stream inside the timed region (the
+    staged path), or from events around the single launch (the fused short-batch path, whose
+    stage kernels are then timed separately for comparison).  With `flush`, L2 is emptied before
+    every step and only the forward itself is inside the events.  Returns the measurements and
+    the resident tensors (for the end-to-end leg and the CPU baseline)."""
     stream = torch.cuda.current_stream()
     inp = W.make_layer_inputs(wl, dev)
     x, logits, gate, up, down = (inp[k] for k in ("x", "logits", "gate", "up", "down"))
     out = torch.empty_like(x)
     wsb = moe.forward_workspace_bytes(wl.T, wl.E, wl.H, wl.I, wl.top_k, logits.dtype, x.dtype)
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-
     idx, _ = moe.moe_route(logits, wl.top_k, wl.renormalize)
     counts = torch.bincount(idx.view(torch.int32).flatten().long(), minlength=wl.E)
     n_active = int((counts > 0).sum())
     max_load = int(counts.max())
     del idx
-
     # short batches run as one fused launch; the staged path is then timed only for comparison
     fused = moe.moe_forward_fused(wl.T, wl.E, wl.H, wl.I, wl.top_k, logits.dtype, x.dtype)
 
@@ -570,14 +554,13 @@ def run_ours(args):
         if evs:
             evs[1].record(stream)
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         step()
     st = moe.moe_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
-
     n_ev = 2 if fused else 6
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(dev)
     barrier(world)
@@ -585,21 +568,30 @@ def run_ours(args):
     sampler.start()
     time.sleep(0.3)   # let the sampler take its first reading
     t_start.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
+        if flush is not None:
+            flush()
         step(evs[i])
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
-    el_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+    if flush is None:
+        el_ms = t_start.elapsed_time(t_end)
+    else:   # the forwards alone, without the flushes between them
+        el_ms = float(sum(e[0].elapsed_time(e[-1]) for e in evs))
+    el_ms = max_over_ranks(el_ms, world, dev)
     st = moe.moe_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed region")
+    fused_ms = None
     if fused:
         fused_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
         # the staged launches on the same inputs, for comparison only (not the timed steps)
         sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(10)]
         for e in sevs:
+            if flush is not None:
+                flush()
             staged_step(e)
         torch.cuda.synchronize()
         stage_ms = {s: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in sevs]))
@@ -607,45 +599,154 @@ def run_ours(args):
     else:
         stage_ms = {s: float(np.mean([e[j].elapsed_time(e[j + 1]) for e in evs]))
                     for j, s in enumerate(STAGES)}
+    return {"el_ms": el_ms, "stage_ms": stage_ms, "fused": fused, "fused_ms": fused_ms,
+            "n_active": n_active, "max_load": max_load, "clocks": clocks,
+            "tensors": {"x": x, "logits": logits, "gate": gate, "up": up, "down": down,
+                        "out": out, "ws": ws}, "inputs": inp}
 
-    value = replica_throughput(wl.T, args.steps, world, el_ms)
-    pk, pk_src = peaks()
-    work = stage_work(wl, n_active)
+
+def layer_roofline(wl, m, pk, pk_src):
+    """Per-stage figures and the roofline entry of the dominant kernel of one measured layer."""
+    work = stage_work(wl, m["n_active"])
+    stage_ms = m["stage_ms"]
+    region_s = m["el_ms"] / 1e3
+    tpeak, tkind = tensor_peak(pk, m["clocks"], region_s)
     stages = {}
     for s in STAGES:
-        d = {"ms": stage_ms[s]}
+        d = {"ms": stage_ms[s], "gbs": work[s]["bytes"] / (stage_ms[s] / 1e3) / 1e9}
         if "flops" in work[s]:
             d["tflops"] = work[s]["flops"] / (stage_ms[s] / 1e3) / 1e12
-        d["gbs"] = work[s]["bytes"] / (stage_ms[s] / 1e3) / 1e9
+            d["frac"] = d["tflops"] / tpeak
+        else:
+            d["frac"] = d["gbs"] / pk["hbm_gbs"]
         stages[s] = d
-    dom = "gate_up_gemm"
-    if fused:
+    if m["fused"]:
+        x, logits = m["tensors"]["x"], m["tensors"]["logits"]
         es = x.element_size()
         # the layer's own bytes: logits, x, the touched experts' weights, out (x_d, a and y
         # stay in L2 between the phases of the fused launch)
         fbytes = (logits.numel() * logits.element_size() + 2 * wl.T * wl.H * es
-                  + 3 * n_active * wl.H * wl.I * es)
-        staged_stages = stages
-        stages = {"fused_forward": {"ms": fused_ms, "gbs": fbytes / (fused_ms / 1e3) / 1e9},
-                  "staged_path_for_comparison": staged_stages}
-        achieved = fbytes / (fused_ms / 1e3) / 1e9
+                  + 3 * m["n_active"] * wl.H * wl.I * es)
+        fms = m["fused_ms"]
+        achieved = fbytes / (fms / 1e3) / 1e9
+        stages = {"fused_forward": {"ms": fms, "gbs": achieved, "frac": achieved / pk["hbm_gbs"]},
+                  "staged_path_for_comparison": stages}
         roof = {"kernel": "moe_decode_fused (route, dispatch, gate/up, down, combine in one "
                           "cooperative launch)",
                 "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"], "peak_source": f"{pk_src} HBM copy",
                 "traffic": None, "algorithmic_bytes_per_launch": fbytes}
-    else:
-        achieved = stages[dom]["tflops"]
-        peak = pk["bf16_tflops_sustained"]
-        roof = {"kernel": ("moe_experts_tc2<gate/up> (CTA-pair tcgen05 grouped GEMM + SwiGLU)"
-                           if wl.rows >= 128 * wl.E else
-                           "moe_experts_tc<gate/up> (tcgen05 grouped GEMM + SwiGLU)"),
-                "bound": "tensor", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"{pk_src} bf16 sustained",
-                "traffic": recorded_traffic() if wl.name == "skewed" else None,
-                "algorithmic_flops_per_launch": work[dom]["flops"],
-                "algorithmic_bytes_per_launch": work[dom]["bytes"]}
+        return stages, roof
+    dom = "gate_up_gemm"
+    pair = wl.rows >= 128 * wl.E
+    kname = "moe_experts_tc2<gate/up>" if pair else "moe_experts_tc<gate/up>"
+    achieved = stages[dom]["tflops"]
+    traffic = recorded_traffic(kname, wl.name)
+    roof = {"kernel": kname + (" (CTA-pair tcgen05 grouped GEMM + SwiGLU)" if pair
+                               else " (tcgen05 grouped GEMM + SwiGLU)"),
+            "bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
+            "frac": achieved / tpeak,
+            "peak_source": f"{pk_src} bf16 {tkind} (cuBLAS; {tkind} chosen from a "
+                           f"{region_s:.2f} s timed region at a median "
+                           f"{(m['clocks'] or {}).get('sm_mhz', 'unknown')} MHz)",
+            "traffic": traffic,
+            "traffic_over_algorithmic": (traffic / work[dom]["bytes"]) if traffic else None,
+            "algorithmic_flops_per_launch": work[dom]["flops"],
+            "algorithmic_bytes_per_launch": work[dom]["bytes"]}
+    return stages, roof
+
+
+def route_entry(moe, wl, dev, steps, warmup, flush):
+    """moe_route alone on a route-only workload, renormalise on and off, L2 emptied before
+    every launch; GB/s of the algorithmic bytes against the HBM peak."""
+    logits = W.make_logits(wl, dev)
+    idx = torch.empty(wl.T, wl.top_k, dtype=torch.uint32, device=dev)
+    w = torch.empty(wl.T, wl.top_k, dtype=logits.dtype, device=dev)
+    es = logits.element_size()
+    nbytes = wl.T * wl.E * es + wl.T * wl.top_k * (4 + es)
+    pk, pk_src = peaks()
+    res = {}
+    sampler = ClockSampler(dev)
+    sampler.start()
+    time.sleep(0.3)
+    for renorm in (True, False):
+        for _ in range(max(3, warmup)):
+            moe.moe_route(logits, wl.top_k, renorm, idx=idx, w=w)
+        times = []
+        for _ in range(steps):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            moe.moe_route(logits, wl.top_k, renorm, idx=idx, w=w)
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = float(np.mean(times))
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res["renormalize" if renorm else "plain"] = {"ms": ms, "gbs": gbs,
+                                                     "frac": gbs / pk["hbm_gbs"]}
+    clocks = sampler.stop()
+    kern = ("moe_route16_small" if es == 2 and wl.E <= 64 and wl.E % 8 == 0 and wl.top_k <= 8
+            else "moe_route_kernel")
+    return res, {"kernel": kern, "bound": "hbm", "peak": pk["hbm_gbs"], "unit": "GB/s",
+                 "peak_source": f"{pk_src} HBM copy", "algorithmic_bytes_per_launch": nbytes,
+                 "traffic": None}, clocks
+
+
+def other_configs(moe, dev, args):
+    """The other workloads, measured in the same process after the headline one: the route-only
+    sweep, the decode layer (the fused launch, L2 emptied between steps), the prefill layer
+    (staged) and the tiny f32 layer (a correctness workload; its time is reported, its roofline
+    is not meaningful)."""
+    pk, pk_src = peaks()
+    flush = L2Flush(dev)
+    out = {}
+    wl = W.WORKLOADS["route_sweep"]
+    res, roof, clocks = route_entry(moe, wl, dev, max(20, args.steps), args.warmup, flush)
+    out["route_sweep"] = {"workload": f"logits [{wl.T}, {wl.E}] {wl.dtype} N(0, 2^2), "
+                                      f"top_k={wl.top_k}", "variants": res, "roofline": roof,
+                          "l2": "emptied before every launch", "clocks": clocks}
+    torch.cuda.empty_cache()
+    for name, steps, fl in (("decode", max(50, args.steps), flush), ("prefill", args.steps, None),
+                            ("tiny_f32", max(20, args.steps), None)):
+        wl = W.WORKLOADS[name]
+        m = measure_layer(moe, wl, dev, steps, args.warmup, flush=fl)
+        stages, roof = layer_roofline(wl, m, pk, pk_src)
+        ms = m["el_ms"] / steps
+        e = {"workload": f"T={wl.T} H={wl.H} I={wl.I} E={wl.E} top_k={wl.top_k} {wl.dtype}"
+                         + (f" Zipf({wl.zipf_s}) expert bias" if wl.zipf_s else ""),
+             "ms": ms, "tokens_per_s": wl.T / (ms / 1e3), "steps": steps,
+             "path": "fused single launch" if m["fused"] else "staged launches",
+             "active_experts": m["n_active"], "max_rows_per_expert": m["max_load"],
+             "l2": "emptied before every step" if fl is not None else
+                   "inputs larger than L2; no flush",
+             "stages": stages, "roofline": roof, "clocks": m["clocks"]}
+        if name == "tiny_f32":
+            e["roofline"] = None
+            e["note"] = "correctness workload (parity in tests/test_gpu_parity.py::test_layer_tiny_f32)"
+        out[name] = e
+        del m
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    import mixture_experts_routing_moe_gb300 as moe
+    from mixture_experts_routing_moe_gb300 import build as build_mod
+    build_mod.build()
+    rank, world, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = W.WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream()
+    m = measure_layer(moe, wl, dev, args.steps, args.warmup, world=world)
+    t = m["tensors"]
+    x, logits, gate, up, down, out, ws = (t[k] for k in ("x", "logits", "gate", "up", "down",
+                                                         "out", "ws"))
+    el_ms = m["el_ms"]
+    value = replica_throughput(wl.T, args.steps, world, el_ms)
+    pk, pk_src = peaks()
+    stages, roof = layer_roofline(wl, m, pk, pk_src)
 
     # End to end through the public API, as a serving loop runs it: every step copies its own
     # inputs in from pinned host memory and its output back to pinned host memory.  Steps are
@@ -702,12 +803,21 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        host = host_storage(inp)
+        host = host_storage(m["inputs"])
         done, secs = time_oracle(wl, host, args.cpu_seconds)
         cores = os.cpu_count()
         cpu = {"value": done / secs, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"first {done} tokens of the {wl.name} workload through the fp64 numpy "
                          f"oracle end to end ({secs:.1f} s; BLAS threads = all {cores} host cores)"}
+        del host
+    n_active, max_load, clocks, fused = m["n_active"], m["max_load"], m["clocks"], m["fused"]
+    x_mb, w_gb = x.numel() * 2 / 1e6, 3 * gate.numel() * 2 / 1e9
+    del m, t, x, logits, gate, up, down, out, ws, xs, ls, outs, x_h, l_h, o_h
+    torch.cuda.empty_cache()
+
+    configs = None
+    if rank == 0 and world == 1 and not args.no_configs:
+        configs = other_configs(moe, dev, args)
 
     if rank == 0:
         line = {
@@ -720,7 +830,7 @@ def run_ours(args):
                        "tokens_per_step_per_gpu": wl.T, "active_experts": n_active,
                        "max_rows_per_expert": max_load,
                        "l2": "inputs larger than L2 (x %.0f MB, weights %.1f GB); no flush" % (
-                           x.numel() * 2 / 1e6, 3 * gate.numel() * 2 / 1e9),
+                           x_mb, w_gb),
                        "parallelism": f"replicas x{world}"},
             "roofline": roof,
             "stages": stages,
@@ -729,6 +839,7 @@ def run_ours(args):
             "e2e": e2e,
             "gpu_launches": (1 if fused else kernels_per_forward(wl)) * args.steps,
             "clocks": clocks,
+            "configs": configs,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

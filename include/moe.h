@@ -160,8 +160,10 @@ int moe_dispatch(const void* x, int xdt, int64_t T, int64_t H, const uint32_t* i
  * the process exits; it allocates nothing (no cudaMalloc, cudaFree or allocating library call).
  * Sizes needing more than that (moe_dispatch_workspace_bytes(T, E, top_k) > the capacity, e.g.
  * T * top_k = 131072 with E = 1024) are rejected with MOE_ERR_SHAPE before anything is enqueued.
- * The first call on a device looks up the array's device address (cudaGetSymbolAddress, once per
- * device, with that device current); make that first call before any stream capture.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current); make that first call before any stream capture.  The address is kept
+ * per device and looked up again only when the device's context has changed (after a
+ * cudaDeviceReset, for example); make the first call after such a change before any capture too.
  * All calls share the one array: calls whose work overlaps on the GPU (different streams, or
  * several host threads) race on it and must be serialised by the caller.  Ids >= E are handled
  * as in moe_dispatch (row_of_slot 0xFFFFFFFF); the device status word is not exposed.
@@ -251,8 +253,11 @@ int moe_forward_sigmoid_grouped(const void* x, const void* logits, int ldt, cons
  * the "cache" of forward_dispatched_training is (x_d, offsets) as returned by moe_dispatch.
  *
  * moe_combine_backward — DispatchedTokens::combine_backward(expert_output, grad_output):
- *   dexpert[row_of_slot[t*k+j]] = w[t, j] * dout[t]   ([T*k, H], dtype ydt; rows of slots whose
+ *   dexpert[row_of_slot[t*k+j]] = w[t, j] * dout[t]   ([T*k, H], dtype ydt; slots whose
  *                                                       row_of_slot is 0xFFFFFFFF are skipped)
+ *   Every row of dexpert is written: row_of_slot as moe_dispatch returns it maps the n valid
+ *   slots onto rows 0 .. n-1, and the T*k - n rows after them (present only when some expert ids
+ *   were invalid) are set to zero, so dexpert needs no initialisation by the caller.
  *   dweights[t, j] = sum_h dout[t, h] * y[row_of_slot[t*k+j], h]   ([T, k] FP32, NaN for such slots)
  *   y [T*k, H] the expert output, w [T, k] the routing weights (dtype wdt), dout [T, H] dtype ydt.
  */

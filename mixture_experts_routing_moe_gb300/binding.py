@@ -335,7 +335,7 @@ def moe_combine_backward(y, row_of_slot, w, dout, stream=None):
     _cuda(y, row_of_slot, w, dout)
     T, k = w.shape
     H = y.shape[1]
-    dexpert = torch.zeros_like(y)
+    dexpert = torch.empty_like(y)
     dweights = torch.empty(T, k, dtype=torch.float32, device=y.device)
     _check(lib().moe_combine_backward(_ptr(y), _code(y), _ptr(row_of_slot), _ptr(w), _code(w),
                                       _ptr(dout), T, H, k, _ptr(dexpert), _ptr(dweights),

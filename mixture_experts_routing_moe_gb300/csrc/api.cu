@@ -1,6 +1,7 @@
 // C-ABI entry points of libmoe (declared in include/moe.h): host-side validation, workspace
 // layout and the launch sequence.  No entry point allocates, frees or synchronises, except
 // moe_device_status, whose job is to read the device status word back.
+#include <atomic>
 #include <math.h>
 #include <string.h>
 
@@ -117,17 +118,18 @@ bool takes_fused(const RouteSpec& rs, int64_t T, int64_t E, int64_t H, int64_t I
   if (!valid_dtype(ldt) || !valid_dtype(wdt)) return false;
   if (E > kFusedDecodeMaxExperts || H > INT32_MAX || I > INT32_MAX) return false;
   if (!fused_decode_supported(T, (int)E, H, I, top_k, ldt, wdt)) return false;
-  static int coop[64] = {};  // 1: cooperative launch supported, 2: not (per device)
+  // 1: cooperative launch supported, 2: not (per device; relaxed atomics, host threads may race
+  // on the first query and every one stores the same value)
+  static std::atomic<int> coop[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  if (coop[dev] == 0) {
+  int c = coop[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
     int v = 0;
-    coop[dev] = (cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess &&
-                 v)
-                    ? 1
-                    : 2;
+    c = (cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && v) ? 1 : 2;
+    coop[dev].store(c, std::memory_order_relaxed);
   }
-  return coop[dev] == 1;
+  return c == 1;
 }
 
 int run_forward(const void* x, const void* logits, int ldt, const void* gate, const void* up,

@@ -118,6 +118,29 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Rows of dexpert that no slot maps to.  moe_dispatch gives the n valid slots the rows 0 .. n-1
+// (a bijection), so the rows it leaves unused are the last R - n, one per slot with row
+// 0xFFFFFFFF; they exist only when some expert ids were invalid.  One block counts those slots
+// and zeroes that many trailing rows, so dexpert is fully defined whatever the buffer held.
+template <typename TY>
+__global__ void __launch_bounds__(1024)
+    moe_combine_bwd_zero_tail(const uint32_t* __restrict__ row_of_slot, int64_t R, int64_t H,
+                              TY* __restrict__ dexpert) {
+  __shared__ unsigned long long n_bad;
+  if (threadIdx.x == 0) n_bad = 0;
+  __syncthreads();
+  unsigned long long c = 0;
+  for (int64_t s = threadIdx.x; s < R; s += blockDim.x) c += row_of_slot[s] == kInvalidRow;
+  if (c) atomicAdd(&n_bad, c);
+  __syncthreads();
+  const int64_t first = R - (int64_t)n_bad;  // the first unused row
+  if (first >= R) return;
+  const int64_t n = (R - first) * H;
+  TY* d = dexpert + first * H;
+  const TY z = Dt<TY>::from_f(0.f);
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) d[i] = z;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256)
     moe_dispatch_bwd_kernel(const T* __restrict__ dinput, const uint32_t* __restrict__ row_of_slot,
@@ -354,13 +377,22 @@ template <typename TY>
 cudaError_t combine_bwd_t(const void* y, const uint32_t* ros, const void* w, int wdt,
                           const void* dout, int64_t T_, int64_t H, int k, void* dexpert,
                           float* dweights, cudaStream_t s) {
+  // the unused trailing rows first: a valid slot that maps into them (a row map not made by
+  // moe_dispatch) is then still written by the kernel below
+  moe_combine_bwd_zero_tail<TY><<<1, 1024, 0, s>>>(ros, T_ * k, H, (TY*)dexpert);
+  cudaError_t err = cudaErrorInvalidValue;
   switch (wdt) {
-    case MOE_F32: return combine_bwd_tw<TY, float>(y, ros, w, dout, T_, H, k, dexpert, dweights, s);
-    case MOE_F16: return combine_bwd_tw<TY, __half>(y, ros, w, dout, T_, H, k, dexpert, dweights, s);
+    case MOE_F32:
+      err = combine_bwd_tw<TY, float>(y, ros, w, dout, T_, H, k, dexpert, dweights, s);
+      break;
+    case MOE_F16:
+      err = combine_bwd_tw<TY, __half>(y, ros, w, dout, T_, H, k, dexpert, dweights, s);
+      break;
     case MOE_BF16:
-      return combine_bwd_tw<TY, __nv_bfloat16>(y, ros, w, dout, T_, H, k, dexpert, dweights, s);
+      err = combine_bwd_tw<TY, __nv_bfloat16>(y, ros, w, dout, T_, H, k, dexpert, dweights, s);
+      break;
   }
-  return cudaErrorInvalidValue;
+  return err;
 }
 
 }  // namespace

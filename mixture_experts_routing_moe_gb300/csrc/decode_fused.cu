@@ -403,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ros_ok = 1;
     if (lane == 0) ros_ok = wait_count(ros_count, (unsigned)R, ring.abort_f, p.status);
     ros_ok = __shfl_sync(0xFFFFFFFFu, ros_ok, 0);
+    __syncwarp();  // orders lane 0's acquire before every lane's row_of_slot reads
     for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; ros_ok && it < (int64_t)p.T * wpt;
          it += (int64_t)gridDim.x * kWarps) {
       const int64_t t = (uint32_t)it / (uint32_t)wpt;  // 32-bit division (it < T * wpt)
@@ -417,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
+      __syncwarp();  // each lane's acquire of its row's count before any lane reads the k rows
       combine_warp<TX, TL, true, true, 8>(reinterpret_cast<const TX*>(p.x_d), p.row_of_slot,
                                        reinterpret_cast<const TL*>(p.w), t, p.H, p.k, c,
                                        reinterpret_cast<TX*>(p.out), lane);

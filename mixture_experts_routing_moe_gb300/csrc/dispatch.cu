@@ -17,7 +17,10 @@
 // Batches of at most 4096 slots run steps 1-3 in one block with the histograms in shared memory.
 // Expert ids >= E are not dispatched: their row_of_slot is 0xFFFFFFFF and the status word gets
 // the index bit.  No access goes out of bounds for any id value.
+#include <cuda.h>
+
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "dispatch_core.cuh"
@@ -208,22 +211,52 @@ DispatchPlan dispatch_plan(int64_t R) {
   return p;
 }
 
+// The id of the calling thread's current CUDA context (0 when none is current or the driver
+// entry points are unavailable).  Context ids are unique for the life of the process, so a
+// context that replaces a destroyed one (after cudaDeviceReset) never matches a cached id.
+static unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext*);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
+  static const std::pair<GetCurrentFn, GetIdFn> fns = []() {
+    void* cur = nullptr;
+    void* id = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &cur, 12000, cudaEnableDefault, &q1) !=
+            cudaSuccess || q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &id, 12000, cudaEnableDefault, &q2) !=
+            cudaSuccess || q2 != cudaDriverEntryPointSuccess)
+      return std::pair<GetCurrentFn, GetIdFn>(nullptr, nullptr);
+    return std::pair<GetCurrentFn, GetIdFn>(reinterpret_cast<GetCurrentFn>(cur),
+                                            reinterpret_cast<GetIdFn>(id));
+  }();
+  if (!fns.first || !fns.second) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (fns.first(&ctx) != CUDA_SUCCESS || !ctx || fns.second(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 cudaError_t static_dispatch_scratch(void** ptr) {
   // Host code must not use g_static_dispatch_scratch as an address: that name is a host-side
-  // stand-in.  The device address is looked up once per device, with that device current.
+  // stand-in.  The device address is looked up with the device current, on the first call on
+  // that device, and again whenever the device's context has changed since (a cudaDeviceReset
+  // destroys the context, and the array gets a new address in the next one).
   constexpr int kMaxDevices = 64;
   static std::mutex mu;
   static void* addr[kMaxDevices] = {};
+  static unsigned long long ctx_of[kMaxDevices] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (!addr[dev] || ctx == 0 || ctx != ctx_of[dev]) {
     void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_static_dispatch_scratch);
+    err = cudaGetSymbolAddress(&p, g_static_dispatch_scratch);  // binds the context if needed
     if (err != cudaSuccess) return err;
     addr[dev] = p;
+    ctx_of[dev] = current_context_id();
   }
   *ptr = addr[dev];
   return cudaSuccess;

@@ -24,6 +24,7 @@
 // L2 (evict_last) while the larger one streams through it (evict_normal).
 // Every wait on an mbarrier is bounded (about a second); on expiry the CTA records the timeout in
 // the status word, stops issuing, lets in-flight copies and MMAs land, frees TMEM and exits.
+#include <atomic>
 #include <cuda.h>
 
 #include "common.cuh"
@@ -435,17 +436,18 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUten
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(2);
   // co-resident pairs on this device (queried once per device)
-  static int max_pairs[64] = {};
+  // (relaxed atomics: host threads may race on the first query; every one stores the same value)
+  static std::atomic<int> max_pairs[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (max_pairs[dev] == 0) {
-    int n = 0;
-    err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+  int mp = max_pairs[dev].load(std::memory_order_relaxed);
+  if (mp == 0) {
+    err = cudaOccupancyMaxActiveClusters(&mp, kern, &cfg);
     if (err != cudaSuccess) return err;
-    if (n < 1) return cudaErrorLaunchOutOfResources;
-    max_pairs[dev] = n;
+    if (mp < 1) return cudaErrorLaunchOutOfResources;
+    max_pairs[dev].store(mp, std::memory_order_relaxed);
   }
   const int64_t upper = ((rows + BM2 - 1) / BM2 + p.E) * (int64_t)p.NT;  // >= number of tiles
-  const int pairs = (int)(upper < max_pairs[dev] ? upper : max_pairs[dev]);
+  const int pairs = (int)(upper < mp ? upper : mp);
   cfg.gridDim = dim3(2 * pairs);
   return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, p);
 }

@@ -10,10 +10,9 @@
 // Persistent clusters of two CTAs (one per SM), the warp roles of the forward kernel (TMA
 // producer, MMA issuer, four epilogue warps), 128 x 256 tiles, 4 x 48 KB stages, FP32
 // accumulators in TMEM.  The two CTAs of a cluster take two tiles of the same expert that share
-// an operand: two m-tiles of one n-tile (each CTA loads its own A tile and one half of B, which
-// TMA multicasts into both CTAs: 32 KB instead of 48 KB read from L2 per 64-deep K block), or,
-// on an expert's odd last m-tile, two n-tiles of it (A halves multicast, own B).  A stage is
-// refilled once the MMAs of both CTAs have consumed it (the commits are multicast).  An
+// an operand: two m-tiles of one n-tile, or, on an expert's odd last m-tile, two n-tiles of it.
+// Each CTA loads all of its own operands (plain TMA loads into its own shared memory); the pair
+// reads the shared operand at about the same time, so the second read is served by L2.  An
 // operand whose contiguous dimension is M or N is loaded as 64-column boxes and described as an
 // MN-major 128-byte-swizzled matrix (boxes 8 KB apart, 8-row groups 1 KB apart).  In WG the last
 // 64-row K block of an expert would run into the next expert's rows: the MMA warp zeroes those
@@ -21,6 +20,7 @@
 // chunk in shared memory (128-byte swizzle) and write it with a TMA tensor store through a
 // [E][M][N] map, so every store moves whole 128-byte lines and never crosses into the next
 // expert's slice.  All waits are bounded as in the forward.
+#include <atomic>
 #include <type_traits>
 
 #include "common.cuh"
@@ -93,8 +93,7 @@ struct BwdParams {
 // expert's last m-tile or n-tile is computed on rows or columns of no interest and not stored.
 template <int MODE>
 __device__ __forceinline__ void decode(int t, const int* pref, const BwdParams& p, uint32_t rank,
-                                       int& e, int& r0, int& r1, int& m, int& n, bool& share_a) {
-  share_a = false;
+                                       int& e, int& r0, int& r1, int& m, int& n) {
   if (MODE == WG) {  // t: position in the tile list of the experts sorted by rows
     const int per = p.MP * p.NT;
     const int sidx = t / per;
@@ -118,7 +117,6 @@ __device__ __forceinline__ void decode(int t, const int* pref, const BwdParams& 
     } else {
       m = mt - 1;
       n = 2 * (local - full) + (int)rank;
-      share_a = true;
     }
   }
 }
@@ -224,7 +222,7 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 2);  // the MMA commits of both CTAs
+      mbar_init(empty_bar(s), 1);  // this CTA's MMA commit
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -240,10 +238,10 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
     tma_prefetch(&mapA);
     tma_prefetch(&mapB0);
     tma_prefetch(&mapB1);
-    tma_prefetch(&mapX);
+    if (MODE == WG) tma_prefetch(&mapX);
   }
   tc_fence_before();
-  cluster_sync_all();  // both CTAs: barriers initialised before any multicast reaches them
+  cluster_sync_all();  // both CTAs started (the tile list is split by cluster rank)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = MODE == WG ? p.E * p.MP * p.NT : pref[p.E];
@@ -259,8 +257,7 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
         const int t = tile_at<MODE>(j, pair, npairs, total);
         if (t < 0) break;
         int e, r0, r1, m, n;
-        bool share_a;
-        decode<MODE>(t, pref, p, rank, e, r0, r1, m, n, share_a);
+        decode<MODE>(t, pref, p, rank, e, r0, r1, m, n);
         const int KB = MODE == WG ? (r1 - r0 + BK - 1) / BK : p.KB;
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_f, p.status)) {
@@ -273,27 +270,14 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
             const int y = r0 + kb * BK;
             for (int j = 0; j < 2; ++j)
               tma_load_2d(sa + j * BOX_BYTES, &mapA, full_bar(stage), p.a_col0 + m * BM + 64 * j, y, pol);
-            for (int j = 2 * (int)rank; j < 2 * (int)rank + 2; ++j)  // this CTA's half of B
-              tma_load_2d_mc(sb + j * BOX_BYTES, &mapB0, full_bar(stage), n * BN + 64 * j, y,
-                             0x3, pol);
+            for (int j = 0; j < 4; ++j)  // B: columns n * BN .. + 255 (four 64-column boxes)
+              tma_load_2d(sb + j * BOX_BYTES, &mapB0, full_bar(stage), n * BN + 64 * j, y, pol);
           } else {
-            // m-pair: own A tile, half of the shared B.  n-pair: half of the shared A (64 rows,
-            // through the 64-row map), own B.
-            if (share_a)
-              tma_load_2d_mc(sa + rank * (A_BYTES / 2), &mapX, full_bar(stage), kb * BK,
-                             r0 + m * BM + 64 * (int)rank, 0x3, pol);
-            else
-              tma_load_2d(sa, &mapA, full_bar(stage), kb * BK, r0 + m * BM, pol);
-            const int jb0 = share_a ? 0 : 2 * (int)rank, jb1 = share_a ? 4 : jb0 + 2;
+            tma_load_2d(sa, &mapA, full_bar(stage), kb * BK, r0 + m * BM, pol);
             if (MODE == GU) {  // K-major: 128 gate rows then the same 128 up rows
               const int br = e * p.I + n * (BN / 2);
-              if (share_a) {
-                tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, br, pol);
-                tma_load_2d(sb + B_BYTES / 2, &mapB1, full_bar(stage), kb * BK, br, pol);
-              } else {  // rank 0 loads the gate half, rank 1 the up half
-                tma_load_2d_mc(sb + rank * (B_BYTES / 2), rank == 0 ? &mapB0 : &mapB1,
-                               full_bar(stage), kb * BK, br, 0x3, pol);
-              }
+              tma_load_2d(sb, &mapB0, full_bar(stage), kb * BK, br, pol);
+              tma_load_2d(sb + B_BYTES / 2, &mapB1, full_bar(stage), kb * BK, br, pol);
             } else {
               // N-major B: rows are K.  DA: down [E*H, I];  DIN: gate (k < I) / up (k >= I)
               const CUtensorMap* mb = &mapB0;
@@ -305,13 +289,8 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
                 if (k0 >= p.I) mb = &mapB1;
                 kr = e * p.I + (k0 >= p.I ? k0 - p.I : k0);
               }
-              for (int j = jb0; j < jb1; ++j) {  // all of B (n-pair) or this CTA's half
-                if (share_a)
-                  tma_load_2d(sb + j * BOX_BYTES, mb, full_bar(stage), n * BN + 64 * j, kr, pol);
-                else
-                  tma_load_2d_mc(sb + j * BOX_BYTES, mb, full_bar(stage), n * BN + 64 * j, kr,
-                                 0x3, pol);
-              }
+              for (int j = 0; j < 4; ++j)
+                tma_load_2d(sb + j * BOX_BYTES, mb, full_bar(stage), n * BN + 64 * j, kr, pol);
             }
           }
           ++armed;
@@ -343,8 +322,7 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
       const int t = tile_at<MODE>(j, pair, npairs, total);
       if (t < 0) break;
       int e, r0, r1, m, n;
-      bool share_a;
-      decode<MODE>(t, pref, p, rank, e, r0, r1, m, n, share_a);
+      decode<MODE>(t, pref, p, rank, e, r0, r1, m, n);
       const int KB = MODE == WG ? (r1 - r0 + BK - 1) / BK : p.KB;
       bool ok = lane != 0 || wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_f, p.status);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
@@ -386,7 +364,7 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
             if (kk < nkk)
               umma_f16(d_tmem, da + (A_MN ? 128u : 2u) * kk, db + (B_MN ? 128u : 2u) * kk, idesc,
                        (kb | kk) != 0);
-          umma_commit_mc(empty_bar(stage), 0x3);  // frees the stage in both CTAs
+          umma_commit(empty_bar(stage));  // frees the stage once its MMAs complete
         }
         __syncwarp();
         if (++stage == NST) {
@@ -413,8 +391,7 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
       const int t = tile_at<MODE>(j, pair, npairs, total);
       if (t < 0) break;
       int e, r0, r1, m, n;
-      bool share_a;
-      decode<MODE>(t, pref, p, rank, e, r0, r1, m, n, share_a);
+      decode<MODE>(t, pref, p, rank, e, r0, r1, m, n);
       const bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_f, p.status);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
@@ -545,7 +522,7 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
 
   tc_fence_before();
   __syncwarp();
-  cluster_sync_all();  // no CTA leaves while its pair may still write to it or signal it
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
@@ -553,8 +530,8 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
 }
 
 // Launches clusters of two CTAs, at most as many as can be resident at once (queried once per
-// device and mode); `upper_pairs` bounds the number of pair tiles.  `x` is the TMA store map of
-// the weight gradient (WG) or the 64-row-box map of A that n-pair tiles load halves through.
+// device and mode); `upper_pairs` bounds the number of pair tiles.  `c` is the TMA store map of
+// the weight gradient (WG; other modes do not read it).
 template <int MODE, bool BF16>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                         const CUtensorMap& c, const BwdParams& p, int64_t upper_pairs, int dev,
@@ -576,16 +553,17 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUten
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3(2);
-  static int max_pairs[64] = {};
+  // (relaxed atomics: host threads may race on the first query; every one stores the same value)
+  static std::atomic<int> max_pairs[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (max_pairs[dev] == 0) {
-    int n = 0;
-    err = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+  int mp = max_pairs[dev].load(std::memory_order_relaxed);
+  if (mp == 0) {
+    err = cudaOccupancyMaxActiveClusters(&mp, kern, &cfg);
     if (err != cudaSuccess) return err;
-    if (n < 1) return cudaErrorLaunchOutOfResources;
-    max_pairs[dev] = n;
+    if (mp < 1) return cudaErrorLaunchOutOfResources;
+    max_pairs[dev].store(mp, std::memory_order_relaxed);
   }
-  const int pairs = (int)(upper_pairs < max_pairs[dev] ? upper_pairs : max_pairs[dev]);
+  const int pairs = (int)(upper_pairs < mp ? upper_pairs : mp);
   if (pairs < 1) return cudaSuccess;
   cfg.gridDim = dim3(2 * pairs);
   return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, c, p);
@@ -605,7 +583,6 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
   uint8_t* abuf = dgdu + align_up((size_t)rows * 2 * I * 2, 256);
   int* order = (int*)(abuf + align_up((size_t)rows * I * 2, 256));  // [E] for the WG tile order
   const int64_t mt_upper = (rows + BM - 1) / BM + E;  // >= m-tiles; pair tiles <= mt * ceil(NT/2)
-  CUtensorMap mAh;  // A with 64-row boxes: the halves of a shared A tile
   CUtensorMap mA, mB0, mB1;
   BwdParams p{};
   p.offsets = offsets;
@@ -616,18 +593,16 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
 
   // 1. da = dy down_e
   if (!make_map_2d(&mA, dy, BF16, H, rows, BK, BM) ||
-      !make_map_2d(&mAh, dy, BF16, H, rows, BK, BM / 2) ||
       !make_map_2d(&mB0, down, BF16, I, (int64_t)E * H, 64, 64))
     return cudaErrorInvalidValue;
   p.KB = (H + BK - 1) / BK;
   p.NT = (I + BN - 1) / BN;
   p.out0 = da;
-  err = launch_mode<DA, BF16>(mA, mB0, mB0, mAh, p, mt_upper * ((p.NT + 1) / 2), dev, s);
+  err = launch_mode<DA, BF16>(mA, mB0, mB0, mA, p, mt_upper * ((p.NT + 1) / 2), dev, s);
   if (err != cudaSuccess) return err;
 
   // 2. g, u recomputed; epilogue -> dg | du, a
   if (!make_map_2d(&mA, x_d, BF16, H, rows, BK, BM) ||
-      !make_map_2d(&mAh, x_d, BF16, H, rows, BK, BM / 2) ||
       !make_map_2d(&mB0, gate, BF16, H, (int64_t)E * I, BK, BN / 2) ||
       !make_map_2d(&mB1, up, BF16, H, (int64_t)E * I, BK, BN / 2))
     return cudaErrorInvalidValue;
@@ -636,19 +611,18 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
   p.da = da;
   p.out0 = dgdu;
   p.out1 = abuf;
-  err = launch_mode<GU, BF16>(mA, mB0, mB1, mAh, p, mt_upper * ((p.NT + 1) / 2), dev, s);
+  err = launch_mode<GU, BF16>(mA, mB0, mB1, mA, p, mt_upper * ((p.NT + 1) / 2), dev, s);
   if (err != cudaSuccess) return err;
 
   // 3. dinput = [dg du] [gate_e; up_e]
   if (!make_map_2d(&mA, dgdu, BF16, 2 * (int64_t)I, rows, BK, BM) ||
-      !make_map_2d(&mAh, dgdu, BF16, 2 * (int64_t)I, rows, BK, BM / 2) ||
       !make_map_2d(&mB0, gate, BF16, H, (int64_t)E * I, 64, 64) ||
       !make_map_2d(&mB1, up, BF16, H, (int64_t)E * I, 64, 64))
     return cudaErrorInvalidValue;
   p.KB = 2 * I / BK;
   p.NT = (H + BN - 1) / BN;
   p.out0 = dinput;
-  err = launch_mode<DIN, BF16>(mA, mB0, mB1, mAh, p, mt_upper * ((p.NT + 1) / 2), dev, s);
+  err = launch_mode<DIN, BF16>(mA, mB0, mB1, mA, p, mt_upper * ((p.NT + 1) / 2), dev, s);
   if (err != cudaSuccess) return err;
 
   // 4. weight gradients, contracted over each expert's rows, experts ordered by row count

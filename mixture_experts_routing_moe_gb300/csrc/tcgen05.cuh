@@ -263,24 +263,6 @@ static __device__ __forceinline__ void umma2_f16(uint32_t d_tmem, uint64_t adesc
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// TMA load multicast to the same shared-memory offset in every CTA of `mask`; each copy signals
-// complete_tx on the mbarrier at offset `bar` of its own CTA.
-static __device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar,
-                                               int x, int y, uint16_t mask, uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(x), "r"(y), "h"(mask), "l"(policy)
-      : "memory");
-}
-// Single-CTA MMAs: arrive on `bar` (same offset) in every CTA of `mask` once they complete.
-static __device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
 // TMA load whose completion is signalled on an mbarrier of either CTA of the pair.
 static __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m,
                                                  uint32_t cluster_bar, int x, int y,

@@ -102,6 +102,44 @@ def test_backward_invalid_slot_gives_nan(ydt, H):
     assert torch.equal(de[r0], ref)
 
 
+@pytest.mark.parametrize("ydt", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("H", [96, 41])
+def test_combine_backward_writes_every_row(ydt, H):
+    """Through the C ABI with an uninitialised dexpert buffer (filled with NaN bytes): ids >= E
+    dispatched by moe_dispatch leave the last rows of the [T*k, H] layout unused; the library
+    sets exactly those to zero and writes w dout into every other row."""
+    from mixture_experts_routing_moe_gb300 import binding as B
+    T, k, E = 50, 4, 6
+    gen = torch.Generator().manual_seed(9)
+    idx = torch.stack([torch.randperm(E + 2, generator=gen)[:k] for _ in range(T)])
+    idx_np = idx.numpy().astype(np.uint32)
+    n_bad = int((idx_np >= E).sum())
+    assert n_bad > 0
+    x = torch.randn(T, 64, generator=gen).to(torch.bfloat16).to(DEV)
+    d = moe.moe_dispatch(x, torch.from_numpy(idx_np.view(np.int32)).to(DEV).view(torch.uint32), E)
+    ros = d["row_of_slot"]
+    y = torch.randn(T * k, H, generator=gen).to(ydt).to(DEV)
+    w = torch.rand(T, k, generator=gen).to(ydt).to(DEV)
+    dout = torch.randn(T, H, generator=gen).to(ydt).to(DEV)
+    de = torch.full((T * k, H), float("nan"), dtype=ydt, device=DEV)
+    dw = torch.empty(T, k, dtype=torch.float32, device=DEV)
+    st = B.lib().moe_combine_backward(y.data_ptr(), B.DTYPE_CODE[ydt], ros.data_ptr(), w.data_ptr(),
+                                      B.DTYPE_CODE[ydt], dout.data_ptr(), T, H, k, de.data_ptr(),
+                                      dw.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    de = de.float().cpu()
+    n_valid = T * k - n_bad
+    assert torch.equal(de[n_valid:], torch.zeros(n_bad, H))
+    ros_np = ros.view(torch.int32).cpu().numpy().view(np.uint32)
+    for s in range(T * k):
+        r = int(ros_np[s])
+        if r != 0xFFFFFFFF:
+            t, j = divmod(s, k)
+            ref = (w[t, j].float().cpu() * dout[t].float().cpu()).to(ydt).float()
+            assert torch.equal(de[r], ref), f"slot {s}"
+
+
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
 def test_full_backward_chain_matches_oracle(dt):
     """forward (route, dispatch, experts, combine) then combine_backward -> experts backward ->

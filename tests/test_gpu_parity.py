@@ -183,11 +183,14 @@ def _expected_dispatch(idx_np, E):
     return counts[:E], offsets[:E + 1], t_of_r[:offsets[E]], r_of_s
 
 
-@pytest.mark.parametrize("case", ["uniform", "zipf", "one_expert", "many_empty", "invalid_ids",
-                                  "large"])
+DISPATCH_SEEDS = {"uniform": 101, "zipf": 102, "one_expert": 103, "many_empty": 104,
+                  "invalid_ids": 105, "large": 106}
+
+
+@pytest.mark.parametrize("case", list(DISPATCH_SEEDS))
 @pytest.mark.parametrize("T0", [1500, 300])   # 6000 slots: multi-block path; 1200: one block
 def test_dispatch_matches_oracle(case, T0):
-    rng = np.random.default_rng(abs(hash(case)) % 2**32)
+    rng = np.random.default_rng(DISPATCH_SEEDS[case] * 10 + (T0 == 300))
     T, E, k, H = T0, 64, 4, 96
     if case == "uniform":
         idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
@@ -296,7 +299,26 @@ def test_experts_match_oracle(dt, case):
 
 
 # ------------------------------------------------------------------------------------ full layer
+def _stratified_tokens(offsets, token_of_row, T, n_total, seed):
+    """A seeded token sample that puts at least one row in every 128-row m-tile of every expert's
+    dispatched group (a random row of each, plus each group's first and last row, so every
+    ragged tail tile is reached), topped up with random tokens to n_total."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            rows += [lo, hi - 1]
+            rows += [int(rng.integers(r0, min(r0 + 128, hi))) for r0 in range(lo, hi, 128)]
+    tok = set(int(t) for t in token_of_row[np.array(rows, dtype=np.int64)])
+    rest = np.setdiff1d(np.arange(T), np.fromiter(tok, dtype=np.int64))
+    extra = max(0, n_total - len(tok))
+    tok |= set(int(t) for t in rng.choice(rest, min(extra, len(rest)), replace=False))
+    return np.array(sorted(tok), dtype=np.int64)
+
+
 def _run_layer(wl, sample=None, seed=0):
+    tok = None
     dev_inputs = W.make_layer_inputs(wl, DEV if sample else "cpu")
     g = {k: v.to(DEV) for k, v in dev_inputs.items()}
     out = moe.moe_forward(g["x"], g["logits"], g["gate"], g["up"], g["down"], wl.top_k,
@@ -318,13 +340,19 @@ def _run_layer(wl, sample=None, seed=0):
     np.testing.assert_array_equal(u32(d["row_of_slot"]), r_of_s)
     np.testing.assert_array_equal(u32(d["token_of_row"]), t_of_r)
     wname = DT_NAME[g["x"].dtype]
+    if sample == "stratified":
+        tok = _stratified_tokens(offsets, t_of_r, wl.T, 2048, seed)
+        print(f"{wl.name}: oracle sample of {len(tok)} tokens covering every (expert, 128-row "
+              f"m-tile) of {int((np.diff(offsets) > 0).sum())} routed experts")
+        sample = len(tok)
     if sample is None:
         st = {k: storage(v) for k, v in dev_inputs.items()}
         ref = O.forward(*st["x"], *st["logits"], st["gate"][0], st["up"][0], st["down"][0],
                         wname, wl.top_k, wl.renormalize)["out_unrounded"]
         got = f64(out)
     else:
-        tok = np.sort(np.random.default_rng(seed).choice(wl.T, sample, replace=False))
+        if tok is None:
+            tok = np.sort(np.random.default_rng(seed).choice(wl.T, sample, replace=False))
         xs = O.to_f64(storage(g["x"][torch.from_numpy(tok).to(DEV)])[0], wname)
         ref = O.forward_rows(xs, ridx[tok], rw[tok],
                              oracle_expert_weights(g["gate"], g["up"], g["down"], wname))
@@ -348,11 +376,14 @@ def test_layer_decode_full():
 
 
 def test_layer_prefill_sampled():
-    _run_layer(W.WORKLOADS["prefill"], sample=48, seed=4)
+    """The prefill layer at full size, checked on >= 2048 tokens that cover every m-tile."""
+    _run_layer(W.WORKLOADS["prefill"], sample="stratified", seed=4)
 
 
 def test_layer_skewed_sampled():
-    _run_layer(W.WORKLOADS["skewed"], sample=16, seed=5)
+    """The skewed layer at full size, checked on >= 2048 tokens that cover every (expert, m-tile),
+    including every ragged tail tile and the last tiles of the heaviest expert."""
+    _run_layer(W.WORKLOADS["skewed"], sample="stratified", seed=5)
 
 
 # ------------------------------------------------------------------------------------ edges
