@@ -271,6 +271,11 @@ EXPERT_CASES = [
     ([37] * 16, 512, 1024),
     ([0, 0, 5, 0], 64, 64),
     ([2100, 3, 250, 0, 0, 640], 384, 1536),    # > 16 m-tiles: two raster groups
+    # CTA-pair path (>= 128 rows per expert on average) with every kind of partial m-tile:
+    # 1..255 rows (operand-swapped tiles, N = rows rounded up to 16), exactly 256, 257; K tail
+    # of the down GEMM (I = 136) and ragged output columns (I = 136, H = 200)
+    ([1, 15, 16, 17, 31, 33, 129, 255, 256, 257, 600, 0], 200, 136),
+    ([5000, 40, 3, 700, 1], 512, 1024),
 ]
 
 
