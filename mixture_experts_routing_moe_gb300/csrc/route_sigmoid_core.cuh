@@ -117,7 +117,7 @@ __device__ __forceinline__ bool sigmoid_row_fp32(const T* __restrict__ src,
       if (g < 64 ? (chosen_lo >> g) & 1ull : (chosen_hi >> (g - 64)) & 1ull) avail |= 1u << i;
     }
   }
-  float prev = 0.f;
+  float prev = 0.f, px = 0.f, pb = 0.f;
   int my_id = -1;
   for (int r = 0; r < k + (k < cand ? 1 : 0); ++r) {
     float bv = -INFINITY;
@@ -131,9 +131,14 @@ __device__ __forceinline__ bool sigmoid_row_fp32(const T* __restrict__ src,
       }
     }
     warp_argmax_f(bv, bi);
-    if (r > 0 && !(prev - bv > 2.f * ec)) return false;
+    // the previous winner beats this one by the margin, or the two have the same logit and the
+    // same correction (then the same score in any precision: the lower id, taken first, wins)
+    const float wx = Dt<T>::to_f(src[bi]), wb = bias ? bias[bi] : 0.f;
+    if (r > 0 && !(prev - bv > 2.f * ec) && !(bv == prev && wx == px && wb == pb)) return false;
     if (r == k) break;
     prev = bv;
+    px = wx;
+    pb = wb;
     if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
     if (lane == r) my_id = bi;  // slot r's expert lives in lane r (k <= 32 here)
   }

@@ -16,6 +16,10 @@ DEV = "cuda"
 CASES = [  # E, groups, selected, top_k, top_two
     (256, 8, 4, 8, True), (64, 8, 3, 6, True), (32, 4, 1, 8, False), (48, 1, 1, 5, False),
     (128, 16, 16, 16, True), (8, 4, 2, 3, False), (1024, 128, 8, 64, True), (96, 3, 2, 40, False),
+    # sub-warp rows (L lanes x EPL experts): L = 32 with 8 and 16 experts a lane, L = 1, 2, 4,
+    # and top_k equal to the candidates of the chosen groups (no (k+1)-th round)
+    (256, 32, 8, 8, True), (512, 8, 2, 8, True), (16, 1, 1, 1, False), (32, 2, 1, 2, True),
+    (64, 4, 2, 4, False), (64, 8, 1, 8, False),
 ]
 
 
