@@ -152,9 +152,15 @@ __device__ __forceinline__ int tile_at(int j, int pair, int P, int N) {
 }
 
 // Experts by descending row count, ties to the lower id (one block, E <= 1024): the order the WG
-// tile list follows.
+// tile list follows.  order[E] = the number of experts with rows (they come first).
 __global__ void __launch_bounds__(1024) moe_expert_order(const int32_t* __restrict__ offsets, int E,
                                                          int* __restrict__ order) {
+  __shared__ int n_active;
+  if (threadIdx.x == 0) n_active = 0;
+  __syncthreads();
+  int mine = 0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) mine += offsets[i + 1] > offsets[i];
+  if (mine) atomicAdd(&n_active, mine);
   __shared__ unsigned long long key[1024];
   int n = 1;
   while (n < E) n <<= 1;
@@ -180,6 +186,23 @@ __global__ void __launch_bounds__(1024) moe_expert_order(const int32_t* __restri
   }
   for (int i = threadIdx.x; i < E; i += blockDim.x)
     order[i] = (int)(0xFFFFFFFFu - (uint32_t)(key[i] & 0xFFFFFFFFull));
+  if (threadIdx.x == 0) order[E] = n_active;
+}
+
+// The weight gradients of experts without rows are zero: written here with 16-byte stores at the
+// HBM write rate, instead of as GEMM tiles.  Block (e, m, j) covers slice j of matrix m (dgate,
+// dup, ddown) of expert e; blocks of experts with rows return at once.
+__global__ void __launch_bounds__(256)
+    moe_zero_idle_grads(const int32_t* __restrict__ offsets, float* __restrict__ g0,
+                        float* __restrict__ g1, float* __restrict__ g2, int64_t per_expert) {
+  const int e = blockIdx.x;
+  if (offsets[e + 1] > offsets[e]) return;
+  float* g = (blockIdx.y == 0 ? g0 : blockIdx.y == 1 ? g1 : g2) + (size_t)e * per_expert;
+  const int64_t n4 = per_expert / 4;  // per_expert = I * H, a multiple of 64
+  float4* v = reinterpret_cast<float4*>(g);
+  for (int64_t i = (int64_t)blockIdx.z * blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.z * blockDim.x)
+    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // Pair tiles of an expert with n rows (modes other than WG).
@@ -244,7 +267,9 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
   cluster_sync_all();  // both CTAs started (the tile list is split by cluster rank)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = MODE == WG ? p.E * p.MP * p.NT : pref[p.E];
+  // WG: the experts with rows only (order[E] of them, first in the order); the others' gradients
+  // are zeroed by moe_zero_idle_grads
+  const int total = MODE == WG ? __ldg(p.order + p.E) * p.MP * p.NT : pref[p.E];
 
   if (warp == 0) {
     if (lane == 0) {
@@ -581,7 +606,7 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
   float* da = (float*)scratch;
   uint8_t* dgdu = (uint8_t*)scratch + align_up((size_t)rows * I * 4, 256);
   uint8_t* abuf = dgdu + align_up((size_t)rows * 2 * I * 2, 256);
-  int* order = (int*)(abuf + align_up((size_t)rows * I * 2, 256));  // [E] for the WG tile order
+  int* order = (int*)(abuf + align_up((size_t)rows * I * 2, 256));  // [E + 1] for the WG tile order
   const int64_t mt_upper = (rows + BM - 1) / BM + E;  // >= m-tiles; pair tiles <= mt * ceil(NT/2)
   CUtensorMap mA, mB0, mB1;
   BwdParams p{};
@@ -625,8 +650,13 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
   err = launch_mode<DIN, BF16>(mA, mB0, mB1, mA, p, mt_upper * ((p.NT + 1) / 2), dev, s);
   if (err != cudaSuccess) return err;
 
-  // 4. weight gradients, contracted over each expert's rows, experts ordered by row count
+  // 4. weight gradients, contracted over each expert's rows, experts ordered by row count; the
+  // zero gradients of experts without rows by a fill
   moe_expert_order<<<1, 1024, 0, s>>>(offsets, E, order);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  moe_zero_idle_grads<<<dim3((unsigned)E, 3, 32), 256, 0, s>>>(offsets, dgate, dup, ddown,
+                                                                (int64_t)I * H);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   p.order = order;
@@ -666,7 +696,7 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
 
 size_t experts_backward_tc_scratch_bytes(int64_t rows, int64_t I) {
   return align_up((size_t)rows * I * 4, 256) + align_up((size_t)rows * 2 * I * 2, 256) +
-         align_up((size_t)rows * I * 2, 256) + 1024 * sizeof(int);
+         align_up((size_t)rows * I * 2, 256) + (1024 + 1) * sizeof(int);
 }
 
 cudaError_t launch_experts_backward_tc(const void* x_d, const int32_t* offsets, int64_t rows,
