@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // An expert's last tile with at most 128 rows runs as M = 128 (64 rows per CTA): each CTA's TMEM
 // lanes 0-63 then hold its 64 rows for N columns 0-127 and lanes 64-127 the same rows for N
 // columns 128-255, in TMEM columns 0-127 (layout measured on GB300).  This keeps the padding of
-// ragged experts at 128-row granularity.  With half of B per CTA a stage is 32 KB, so six stages fit, and each CTA pulls a
+// ragged experts at 128-row granularity; such a tile's CTAs load 64 A rows each (a 64-row map).  With half of B per CTA a stage is 32 KB, so six stages fit, and each CTA pulls a
 // third fewer bytes per FLOP through L2 than a single-CTA 128 x 256 tile.
 // Synchronisation: both CTAs' TMA loads signal CTA 0's full barrier (CTA 0 arms it for both);
 // CTA 0's MMA commits are multicast to the empty / tmem-full barriers of both CTAs; all eight
@@ -116,7 +116,8 @@ template <bool GATEUP, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_experts_tc2(const __grid_constant__ CUtensorMap mapA,
                     const __grid_constant__ CUtensorMap mapB0,
-                    const __grid_constant__ CUtensorMap mapB1, const TcParams p) {
+                    const __grid_constant__ CUtensorMap mapB1,
+                    const __grid_constant__ CUtensorMap mapAh, const TcParams p) {
   extern __shared__ uint8_t tc_smem_raw[];
   const uint32_t raw = smem_u32(tc_smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -158,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch(&mapA);
     tma_prefetch(&mapB0);
     if (GATEUP) tma_prefetch(&mapB1);
+    tma_prefetch(&mapAh);
   }
   tc_fence_before();
   cluster_sync_all();  // both CTAs: barriers initialised, TMEM allocated, prefix built
@@ -188,8 +190,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t sa = base + stage * STAGE2_BYTES, sb = sa + A2_BYTES;
           const uint32_t fb = map_to_rank(full_bar(stage), 0);
-          if (leader) mbar_expect_tx(full_bar(stage), 2 * STAGE2_BYTES);
-          tma_load_2d_pair(sa, &mapA, fb, kb * BK, a_row, pa);
+          // a half tile's CTA loads only its 64 A rows (the MMA reads no more of them)
+          if (leader) mbar_expect_tx(full_bar(stage), 2 * (half ? STAGE2_BYTES - A2_BYTES / 2 : STAGE2_BYTES));
+          tma_load_2d_pair(sa, half ? &mapAh : &mapA, fb, kb * BK, a_row, pa);
           if (GATEUP) {  // 64 gate rows, then the same 64 up rows
             tma_load_2d_pair(sb, &mapB0, fb, kb * BK, b_row, pb);
             tma_load_2d_pair(sb + B2_BYTES / 2, &mapB1, fb, kb * BK, b_row, pb);
@@ -418,7 +421,8 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
 
 template <bool GATEUP, bool BF16>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                        const TcParams& p, int64_t rows, int dev, cudaStream_t s) {
+                        const CUtensorMap& ah, const TcParams& p, int64_t rows, int dev,
+                        cudaStream_t s) {
   auto kern = moe_experts_tc2<GATEUP, BF16>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmem2Bytes);
@@ -449,7 +453,7 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUten
   const int64_t upper = ((rows + BM2 - 1) / BM2 + p.E) * (int64_t)p.NT;  // >= number of tiles
   const int pairs = (int)(upper < mp ? upper : mp);
   cfg.gridDim = dim3(2 * pairs);
-  return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, p);
+  return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, ah, p);
 }
 
 template <bool BF16>
@@ -472,17 +476,19 @@ cudaError_t launch_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, c
     return cudaErrorInvalidValue;
 
   TcParams p1{offsets, (uint8_t*)a, status, E, I, (H + BK - 1) / BK, (I + BN / 2 - 1) / (BN / 2), I};
+  CUtensorMap mxh, mah;  // the pair kernel's half tiles load 64 rows of x_d / a per CTA
   if (pair) {  // the pair kernel loads gate and up in 64-row boxes (interleaved B halves)
     if (!make_map(&mg, gate, BF16, H, (int64_t)E * I, BN / 4) ||
-        !make_map(&mu, up, BF16, H, (int64_t)E * I, BN / 4))
+        !make_map(&mu, up, BF16, H, (int64_t)E * I, BN / 4) ||
+        !make_map(&mxh, x_d, BF16, H, rows, BM / 2) || !make_map(&mah, a, BF16, I, rows, BM / 2))
       return cudaErrorInvalidValue;
   }
-  err = pair ? launch_pair<true, BF16>(mx, mg, mu, p1, rows, dev, s)
+  err = pair ? launch_pair<true, BF16>(mx, mg, mu, mxh, p1, rows, dev, s)
              : launch_one<true, BF16>(mx, mg, mu, p1, rows, sms, s);
   if (err != cudaSuccess) return err;
   if (between && (err = cudaEventRecord(between, s)) != cudaSuccess) return err;
   TcParams p2{offsets, (uint8_t*)y, status, E, H, (I + BK - 1) / BK, (H + BN - 1) / BN, H};
-  return pair ? launch_pair<false, BF16>(ma, md, md, p2, rows, dev, s)
+  return pair ? launch_pair<false, BF16>(ma, md, md, mah, p2, rows, dev, s)
               : launch_one<false, BF16>(ma, md, md, p2, rows, sms, s);
 }
 

@@ -78,6 +78,8 @@ struct BwdParams {
   int MP;           // WG: m-tile pairs per expert
   int M, N;         // WG: output matrix of each expert is M x N
   int a_col0;       // WG: first column of A inside its source matrix (du starts at I)
+  int split;        // WG: rows of C below this go to the map `mapX`, the others (row - split)
+                    // to `mapB1` (dgate | dup in one launch: split = I)
   const int* order; // WG: experts by descending row count (ties: lower id first)
   const float* da;  // GU: da [rows, I] FP32
   void* out0;       // DA: da FP32; GU: dgdu; DIN: dinput; WG: C [E, M, N] FP32
@@ -451,7 +453,10 @@ __global__ void __launch_bounds__(n_threads<MODE>(), 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_3d(&mapX, buf, col0, row0, e);
+              if (row0 < p.split)  // a 32-row chunk never straddles split (a multiple of 64)
+                tma_store_3d(&mapX, buf, col0, row0, e);
+              else
+                tma_store_3d(&mapB1, buf, col0, row0 - p.split, e);
               bulk_commit();
             }
             slot = slot + 1 == kStoreBufs ? 0 : slot + 1;
@@ -660,23 +665,21 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   p.order = order;
-  CUtensorMap mX, mC;
+  // dgate and dup in one launch: [dg du]^T x_d is a [2I, H] matrix per expert, whose rows below
+  // I are dgate's and the others dup's
+  CUtensorMap mX, mC, mC2;
   if (!make_map_2d(&mA, dgdu, BF16, 2 * (int64_t)I, rows, 64, 64) ||
       !make_map_2d(&mX, x_d, BF16, H, rows, 64, 64) ||
-      !make_map_3d_f32(&mC, dgate, H, I, E, 32, 32))
+      !make_map_3d_f32(&mC, dgate, H, I, E, 32, 32) || !make_map_3d_f32(&mC2, dup, H, I, E, 32, 32))
     return cudaErrorInvalidValue;
-  p.M = I;
+  p.M = 2 * I;
+  p.split = I;
   p.N = H;
-  p.MP = (I + 2 * BM - 1) / (2 * BM);
+  p.MP = (2 * I + 2 * BM - 1) / (2 * BM);
   p.NT = (H + BN - 1) / BN;
   p.out0 = dgate;
   p.a_col0 = 0;
-  err = launch_mode<WG, BF16>(mA, mX, mX, mC, p, (int64_t)E * p.MP * p.NT, dev, s);
-  if (err != cudaSuccess) return err;
-  if (!make_map_3d_f32(&mC, dup, H, I, E, 32, 32)) return cudaErrorInvalidValue;
-  p.out0 = dup;
-  p.a_col0 = I;
-  err = launch_mode<WG, BF16>(mA, mX, mX, mC, p, (int64_t)E * p.MP * p.NT, dev, s);
+  err = launch_mode<WG, BF16>(mA, mX, mC2, mC, p, (int64_t)E * p.MP * p.NT, dev, s);
   if (err != cudaSuccess) return err;
   CUtensorMap mY, mAct;
   if (!make_map_2d(&mY, dy, BF16, H, rows, 64, 64) ||
@@ -684,6 +687,7 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
       !make_map_3d_f32(&mC, ddown, I, H, E, 32, 32))
     return cudaErrorInvalidValue;
   p.M = H;
+  p.split = H;
   p.N = I;
   p.MP = (H + 2 * BM - 1) / (2 * BM);
   p.NT = (I + BN - 1) / BN;
