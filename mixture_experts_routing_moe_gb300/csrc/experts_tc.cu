@@ -112,12 +112,28 @@ constexpr int kStage2Out = 32 * 128;
 constexpr size_t kSmem2Bytes = 1024 + (size_t)STAGES2 * STAGE2_BYTES + 256 +
                                (kMaxExperts + 4) * sizeof(int) + 4 * kStage2Out;
 
-template <bool GATEUP, bool BF16>
+// The GEMMs the pair kernel runs.  Forward: gate/up (A = x_d, B = interleaved gate / up halves,
+// a = silu(g) u) and down (A = a, B = down, plain cast).  Expert backward (ruDNN user guide §12):
+//   kDa   da = dy down_e          A = dy [rows, H], B = down_e [H, I] with N (= I) contiguous,
+//                                 FP32 output
+//   kGu   g, u = x_d gate_e^T, x_d up_e^T recomputed as in the forward; epilogue with da:
+//                                 s = sigmoid(g), dg = da u s (1 + g (1 - s)), du = da g s,
+//                                 a = g s u -> dg | du [rows, 2I] and a [rows, I]
+//   kDin  dinput = [dg du] [gate_e; up_e]   A = dg | du [rows, 2I], B = gate_e / up_e [I, H] with
+//                                 N (= H) contiguous (k < I from gate, else up), plain cast
+// A B operand with N contiguous is loaded as two 64-column boxes per CTA half and described as an
+// MN-major 128-byte-swizzled matrix (boxes 8 KB apart).
+enum PairKind { kGateUp = 0, kDown = 1, kDa = 2, kGu = 3, kDin = 4 };
+
+template <int KIND, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_experts_tc2(const __grid_constant__ CUtensorMap mapA,
                     const __grid_constant__ CUtensorMap mapB0,
                     const __grid_constant__ CUtensorMap mapB1,
                     const __grid_constant__ CUtensorMap mapAh, const TcParams p) {
+  constexpr bool GATEUP = KIND == kGateUp || KIND == kGu;  // B: interleaved gate / up halves
+  constexpr bool B_MN = KIND == kDa || KIND == kDin;       // B stored with N contiguous
+  constexpr int ES = KIND == kDa ? 4 : 2;                  // output element size
   extern __shared__ uint8_t tc_smem_raw[];
   const uint32_t raw = smem_u32(tc_smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -158,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch(&mapA);
     tma_prefetch(&mapB0);
-    if (GATEUP) tma_prefetch(&mapB1);
+    if (GATEUP || KIND == kDin) tma_prefetch(&mapB1);
     tma_prefetch(&mapAh);
   }
   tc_fence_before();
@@ -196,8 +212,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (GATEUP) {  // 64 gate rows, then the same 64 up rows
             tma_load_2d_pair(sb, &mapB0, fb, kb * BK, b_row, pb);
             tma_load_2d_pair(sb + B2_BYTES / 2, &mapB1, fb, kb * BK, b_row, pb);
-          } else {
+          } else if (!B_MN) {
             tma_load_2d_pair(sb, &mapB0, fb, kb * BK, b_row, pb);
+          } else {
+            // this CTA's 128 output columns as two 64-column boxes of the 64 K rows of the stage:
+            // down rows e H + k (kDa), or gate rows e I + k for k < I and up rows e I + k - I
+            const CUtensorMap* mb = &mapB0;
+            int kr = e * p.b_rows + kb * BK;
+            if (KIND == kDin) {
+              const int k0 = kb * BK;
+              if (k0 >= p.I) mb = &mapB1;
+              kr = e * p.I + (k0 >= p.I ? k0 - p.I : k0);
+            }
+            const int c0 = n * BN + (int)rank * 128;
+            tma_load_2d_pair(sb, mb, fb, c0, kr, pb);
+            tma_load_2d_pair(sb + B2_BYTES / 2, mb, fb, c0 + 64, kr, pb);
           }
           ++armed;
           if (++stage == STAGES2) {
@@ -221,8 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (leader && lane == 0) {
       // ------------------------------------------------------------ MMA issuer (CTA 0 only)
-      constexpr uint32_t idesc_full = make_idesc(BF16, BM2, BN);
-      constexpr uint32_t idesc_half = make_idesc(BF16, BM2 / 2, BN);
+      constexpr uint32_t bmn = B_MN ? 1u << 16 : 0u;  // instruction descriptor: B MN-major
+      constexpr uint32_t idesc_full = make_idesc(BF16, BM2, BN) | bmn;
+      constexpr uint32_t idesc_half = make_idesc(BF16, BM2 / 2, BN) | bmn;
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool stop = false;
@@ -241,10 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t sa = base + stage * STAGE2_BYTES, sb = sa + A2_BYTES;
-          const uint64_t da = make_sdesc(sa), db = make_sdesc(sb);
+          const uint64_t da = make_sdesc(sa);
+          const uint64_t db = B_MN ? make_sdesc_mn_box(sb, B2_BYTES / 2) : make_sdesc(sb);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            umma2_f16(d_tmem, da + 2u * kk, db + 2u * kk, idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < BK / 16; ++kk)  // K = 16: 32 bytes (K-major) or 2 KB (MN-major)
+            umma2_f16(d_tmem, da + 2u * kk, db + (B_MN ? 128u : 2u) * kk, idesc, (kb | kk) != 0);
           umma_commit2(empty_bar(stage), 0x3);
           if (++stage == STAGES2) {
             stage = 0;
@@ -281,8 +312,88 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nhalf = half ? (q >> 1) : 0;  // which half of N this warp holds (half tiles)
       const bool valid = row < r_end;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      uint8_t* orow = p.out + (size_t)row * p.N * 2;
-      if (GATEUP) {
+      uint8_t* orow = p.out + (size_t)row * p.N * ES;
+      if (KIND == kGu) {
+        // as the gate/up epilogue, with the SwiGLU gradient: dg | du and a for 32 columns at once
+        const float* darow = p.da + (size_t)row * p.I;
+        uint8_t* arow = p.out1 + (size_t)row * p.I * 2;
+        uint8_t* dgrow = p.out + (size_t)row * 2 * p.I * 2;
+#pragma unroll 1
+        for (int j = 0; j < (half ? 2 : 4); ++j) {
+          const int gc = half ? 32 * j : (j & 1) * 32 + (j >> 1) * 128;
+          uint32_t g[32], u[32];
+          tmem_ld32(taddr + gc, g);
+          tmem_ld32(taddr + gc + 64, u);
+          tmem_wait_ld();
+          const int col0 = n * (BN / 2) + (half ? 64 * nhalf + 32 * j : 32 * j);
+          if (valid) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (col0 + v * 8 < p.I) {
+                float dv[8];
+                *reinterpret_cast<uint4*>(dv) = ld_nc_v4(darow + col0 + v * 8);
+                *reinterpret_cast<uint4*>(dv + 4) = ld_nc_v4(darow + col0 + v * 8 + 4);
+                uint32_t pg[4], pu[4], pa[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  float dgv[2], duv[2], av[2];
+#pragma unroll
+                  for (int h = 0; h < 2; ++h) {
+                    const float gv = __uint_as_float(g[v * 8 + i * 2 + h]);
+                    const float uv = __uint_as_float(u[v * 8 + i * 2 + h]);
+                    const float sg = 1.f / (1.f + __expf(-gv));
+                    const float act = gv * sg, d = dv[i * 2 + h];
+                    dgv[h] = d * uv * sg * (1.f + gv * (1.f - sg));
+                    duv[h] = d * act;
+                    av[h] = act * uv;
+                  }
+                  pg[i] = pack2<BF16>(dgv[0], dgv[1]);
+                  pu[i] = pack2<BF16>(duv[0], duv[1]);
+                  pa[i] = pack2<BF16>(av[0], av[1]);
+                }
+                st_v4(dgrow + (size_t)(col0 + v * 8) * 2, make_uint4(pg[0], pg[1], pg[2], pg[3]));
+                st_v4(dgrow + (size_t)(p.I + col0 + v * 8) * 2,
+                      make_uint4(pu[0], pu[1], pu[2], pu[3]));
+                st_v4(arow + (size_t)(col0 + v * 8) * 2, make_uint4(pa[0], pa[1], pa[2], pa[3]));
+              }
+            }
+          }
+        }
+      } else if (KIND == kDa) {
+        // FP32 output.  Full tile with all 32 rows of this warp in the expert: 32-column chunks
+        // (128 bytes a row) staged through shared memory and written as whole 128-byte lines, as
+        // below; otherwise this lane's row, 16 bytes at a time.
+        const bool staged = !half && __all_sync(0xFFFFFFFFu, valid);
+        const uint32_t buf = stage_out + (uint32_t)(q * kStage2Out);
+        const int row0 = r0 + (int)rank * 128 + q * 32;
+#pragma unroll 1
+        for (int c = 0; c < (half ? 4 : 8); ++c) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c * 32, r);
+          tmem_wait_ld();
+          const int col0 = n * BN + 128 * nhalf + c * 32;
+          if (staged && col0 + 32 <= p.N) {
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), r[4 * j], r[4 * j + 1],
+                           r[4 * j + 2], r[4 * j + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int pass = 0; pass < 8; ++pass) {
+              const int rr = pass * 4 + (lane >> 3), ch = lane & 7;
+              const uint4 v = ld_shared_v4(buf + rr * 128 + ((ch ^ (rr & 7)) << 4));
+              st_v4(p.out + ((size_t)(row0 + rr) * p.N + col0 + ch * 4) * 4, v);
+            }
+          } else if (valid) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              if (col0 + v * 4 < p.N)
+                st_v4(orow + (size_t)(col0 + v * 4) * 4,
+                      make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]));
+          }
+        }
+      } else if (GATEUP) {
         // output column group j (32 columns): gate at accumulator column gc, up at gc + 64;
         // full tile: j = 0..3, gc = (j & 1) * 32 + (j >> 1) * 128, outputs n*128 + 32 j;
         // half tile: j = 0..1, gc = 32 j, outputs n*128 + 64 nhalf + 32 j
@@ -419,11 +530,11 @@ cudaError_t launch_one(const CUtensorMap& a, const CUtensorMap& b0, const CUtens
   return cudaGetLastError();
 }
 
-template <bool GATEUP, bool BF16>
+template <int KIND, bool BF16>
 cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                         const CUtensorMap& ah, const TcParams& p, int64_t rows, int dev,
                         cudaStream_t s) {
-  auto kern = moe_experts_tc2<GATEUP, BF16>;
+  auto kern = moe_experts_tc2<KIND, BF16>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmem2Bytes);
   if (err != cudaSuccess) return err;
@@ -483,16 +594,67 @@ cudaError_t launch_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, c
         !make_map(&mxh, x_d, BF16, H, rows, BM / 2) || !make_map(&mah, a, BF16, I, rows, BM / 2))
       return cudaErrorInvalidValue;
   }
-  err = pair ? launch_pair<true, BF16>(mx, mg, mu, mxh, p1, rows, dev, s)
+  err = pair ? launch_pair<kGateUp, BF16>(mx, mg, mu, mxh, p1, rows, dev, s)
              : launch_one<true, BF16>(mx, mg, mu, p1, rows, sms, s);
   if (err != cudaSuccess) return err;
   if (between && (err = cudaEventRecord(between, s)) != cudaSuccess) return err;
   TcParams p2{offsets, (uint8_t*)y, status, E, H, (I + BK - 1) / BK, (H + BN - 1) / BN, H};
-  return pair ? launch_pair<false, BF16>(ma, md, md, mah, p2, rows, dev, s)
+  return pair ? launch_pair<kDown, BF16>(ma, md, md, mah, p2, rows, dev, s)
               : launch_one<false, BF16>(ma, md, md, p2, rows, sms, s);
 }
 
+template <bool BF16>
+cudaError_t bwd_pair_t(const void* x_d, const int32_t* offsets, int64_t rows, const void* gate,
+                       const void* up, const void* down, int E, int H, int I, const void* dy,
+                       float* da, void* dgdu, void* a, void* dinput, unsigned* status,
+                       cudaStream_t s) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  CUtensorMap mA, mAh, mB0, mB1;
+  // 1. da = dy down_e: down read as [E H, I] (N = I contiguous) in 64 x 64 boxes
+  if (!make_map(&mA, dy, BF16, H, rows, BM) || !make_map(&mAh, dy, BF16, H, rows, BM / 2) ||
+      !tc::make_map_2d(&mB0, down, BF16, I, (int64_t)E * H, 64, 64))
+    return cudaErrorInvalidValue;
+  TcParams p1{offsets, (uint8_t*)da, status, E, I, (H + BK - 1) / BK, (I + BN - 1) / BN, H};
+  err = launch_pair<kDa, BF16>(mA, mB0, mB0, mAh, p1, rows, dev, s);
+  if (err != cudaSuccess) return err;
+  // 2. g, u recomputed (gate and up in 64-row K-major boxes, as the forward), SwiGLU gradient
+  if (!make_map(&mA, x_d, BF16, H, rows, BM) || !make_map(&mAh, x_d, BF16, H, rows, BM / 2) ||
+      !make_map(&mB0, gate, BF16, H, (int64_t)E * I, BN / 4) ||
+      !make_map(&mB1, up, BF16, H, (int64_t)E * I, BN / 4))
+    return cudaErrorInvalidValue;
+  TcParams p2{offsets, (uint8_t*)dgdu, status, E, I, (H + BK - 1) / BK, (I + BN / 2 - 1) / (BN / 2), I};
+  p2.da = da;
+  p2.out1 = (uint8_t*)a;
+  p2.I = I;
+  err = launch_pair<kGu, BF16>(mA, mB0, mB1, mAh, p2, rows, dev, s);
+  if (err != cudaSuccess) return err;
+  // 3. dinput = [dg du] [gate_e; up_e]: gate and up read as [E I, H] (N = H contiguous)
+  if (!make_map(&mA, dgdu, BF16, 2 * (int64_t)I, rows, BM) ||
+      !make_map(&mAh, dgdu, BF16, 2 * (int64_t)I, rows, BM / 2) ||
+      !tc::make_map_2d(&mB0, gate, BF16, H, (int64_t)E * I, 64, 64) ||
+      !tc::make_map_2d(&mB1, up, BF16, H, (int64_t)E * I, 64, 64))
+    return cudaErrorInvalidValue;
+  TcParams p3{offsets, (uint8_t*)dinput, status, E, H, 2 * I / BK, (H + BN - 1) / BN, I};
+  p3.I = I;
+  return launch_pair<kDin, BF16>(mA, mB0, mB1, mAh, p3, rows, dev, s);
+}
+
 }  // namespace
+
+cudaError_t launch_experts_bwd_pair(const void* x_d, const int32_t* offsets, int64_t rows,
+                                    const void* gate, const void* up, const void* down, int wdt,
+                                    int E, int H, int I, const void* dy, float* da, void* dgdu,
+                                    void* a, void* dinput, unsigned* status, cudaStream_t s) {
+  if (wdt == MOE_BF16)
+    return bwd_pair_t<true>(x_d, offsets, rows, gate, up, down, E, H, I, dy, da, dgdu, a, dinput,
+                            status, s);
+  if (wdt == MOE_F16)
+    return bwd_pair_t<false>(x_d, offsets, rows, gate, up, down, E, H, I, dy, da, dgdu, a,
+                             dinput, status, s);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_experts_tc(const void* x_d, const int32_t* offsets, int64_t rows,
                               const void* gate, const void* up, const void* down, int wdt, int E,

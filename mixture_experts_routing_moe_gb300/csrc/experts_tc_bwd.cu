@@ -621,6 +621,12 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
   p.I = I;
   p.status = status;
 
+  // 1-3 on CTA pairs (256-row tiles) when the experts average at least 128 rows, as the forward
+  if (rows >= (int64_t)128 * E) {
+    err = launch_experts_bwd_pair(x_d, offsets, rows, gate, up, down, BF16 ? MOE_BF16 : MOE_F16, E,
+                                  H, I, dy, da, dgdu, abuf, dinput, status, s);
+    if (err != cudaSuccess) return err;
+  } else {
   // 1. da = dy down_e
   if (!make_map_2d(&mA, dy, BF16, H, rows, BK, BM) ||
       !make_map_2d(&mB0, down, BF16, I, (int64_t)E * H, 64, 64))
@@ -654,6 +660,7 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
   p.out0 = dinput;
   err = launch_mode<DIN, BF16>(mA, mB0, mB1, mA, p, mt_upper * ((p.NT + 1) / 2), dev, s);
   if (err != cudaSuccess) return err;
+  }
 
   // 4. weight gradients, contracted over each expert's rows, experts ordered by row count; the
   // zero gradients of experts without rows by a fill

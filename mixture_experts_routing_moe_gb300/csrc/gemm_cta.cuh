@@ -83,6 +83,11 @@ struct TcParams {
   const unsigned* ready_wait;
   unsigned ready_target;
   int signal_nt;  // > 0: ready_signal is per (m-tile, n-tile): index (pref[e] + m) * signal_nt + n
+  // CTA-pair kernels of the expert backward: the FP32 da read by the SwiGLU-gradient epilogue,
+  // its second output (a), and the intermediate size I
+  const float* da;
+  uint8_t* out1;
+  int I;
 };
 
 __device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {

@@ -110,6 +110,13 @@ bool fused_decode_supported(int64_t T, int E, int64_t H, int64_t I, int k, int l
 cudaError_t launch_decode_fused(const FusedDecodeArgs& f, int ldt, int wdt, cudaStream_t s);
 
 // bf16 / f16 experts on tcgen05 tensor cores; `a` is an [rows, I] scratch buffer of dtype wdt.
+// Steps 1-3 of the tensor-core expert backward on CTA pairs (256-row tiles, cta_group::2): da =
+// dy down_e (FP32), g and u recomputed with the SwiGLU gradient (dg | du and a in the layer dtype),
+// dinput = [dg du] [gate_e; up_e].  For experts averaging at least 128 rows; I % 64 == 0.
+cudaError_t launch_experts_bwd_pair(const void* x_d, const int32_t* offsets, int64_t rows,
+                                    const void* gate, const void* up, const void* down, int wdt,
+                                    int E, int H, int I, const void* dy, float* da, void* dgdu,
+                                    void* a, void* dinput, unsigned* status, cudaStream_t s);
 cudaError_t launch_experts_tc(const void* x_d, const int32_t* offsets, int64_t rows,
                               const void* gate, const void* up, const void* down, int wdt, int E,
                               int H, int I, void* y, void* a, unsigned* status, cudaStream_t s,

@@ -196,6 +196,14 @@ static __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr) {
          ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Shared-memory descriptor of an MN-major operand (N contiguous) written by TMA as 64-column
+// boxes of 128-byte rows with 128-byte swizzle: boxes `box_bytes` apart (LBO), 8-row groups 1 KB
+// apart (SBO).  One K = 16 step is 16 rows = 2 KB further.
+static __device__ __forceinline__ uint64_t make_sdesc_mn_box(uint32_t saddr, uint32_t box_bytes) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(box_bytes >> 4) << 16) |
+         ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
 template <bool BF16>
 static __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   if (BF16) {

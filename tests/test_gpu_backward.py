@@ -29,7 +29,12 @@ def _groups(counts, seed):
 @pytest.mark.parametrize("counts,H,I", [([70, 0, 129, 5], 96, 160), ([200], 64, 72),
                                         ([33] * 6, 128, 256), ([0, 0, 3, 0], 40, 24),
                                         ([300, 0, 129, 77], 256, 384), ([1000], 128, 192),
-                                        ([0, 40, 0, 513, 2], 200, 128)])
+                                        ([0, 40, 0, 513, 2], 200, 128),
+                                        # >= 128 rows per expert: dA, g/u and dinput on CTA
+                                        # pairs (half tiles of 1, 129 and 44 rows, ragged
+                                        # output columns, dinput's K crossing from gate to up)
+                                        ([600, 0, 1, 257, 129, 256], 192, 256),
+                                        ([2000, 300], 512, 320)])
 def test_experts_backward_matches_oracle(dt, counts, H, I):
     E = len(counts)
     _, offsets, _, _ = O.dispatch(_groups(counts, sum(counts)), E)
