@@ -67,6 +67,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the other workloads measured after the headline one")
+    ap.add_argument("--config-cpu-seconds", type=float, default=3.0,
+                    help="target CPU time of the oracle baseline of each other workload")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward chain (combine, experts, dispatch, router) instead")
     ap.add_argument("--router", choices=["softmax", "sigmoid"], default="softmax",
@@ -696,6 +698,31 @@ def route_entry(moe, wl, dev, steps, warmup, flush):
                  "traffic": None}, clocks
 
 
+def cpu_leg(wl, inputs, seconds):
+    """The oracle, as it stands, on the first tokens of a workload for about `seconds` of CPU time
+    (the same CPU baseline as the headline's, on a smaller sample)."""
+    import oracle as O
+    cores = os.cpu_count()
+    if wl.H == 0:  # route only: grow the row sample
+        arr, name = W.to_storage_numpy(inputs["logits"])
+        n, done, elapsed = 1024, 0, 0.0
+        while elapsed < seconds and done < wl.T:
+            n = min(n, wl.T - done)
+            t0 = time.perf_counter()
+            O.route(O.to_f64(arr[done:done + n], name), wl.top_k, True, name)
+            elapsed += time.perf_counter() - t0
+            done += n
+            n *= 2
+        what = f"route of the first {done} rows"
+    else:
+        host = host_storage(inputs)
+        done, elapsed = time_oracle(wl, host, seconds)
+        what = f"the first {done} tokens end to end"
+    return {"value": done / elapsed, "unit": "tokens/s" if wl.H else "rows/s", "cores": cores,
+            "kind": "oracle", "sample": f"{what} of the {wl.name} workload through the fp64 numpy "
+                                        f"oracle ({elapsed:.1f} s; BLAS threads = all {cores} host cores)"}
+
+
 def other_configs(moe, dev, args):
     """The other workloads, measured in the same process after the headline one: the route-only
     sweep, the decode layer (the fused launch, L2 emptied between steps), the prefill layer
@@ -709,6 +736,9 @@ def other_configs(moe, dev, args):
     out["route_sweep"] = {"workload": f"logits [{wl.T}, {wl.E}] {wl.dtype} N(0, 2^2), "
                                       f"top_k={wl.top_k}", "variants": res, "roofline": roof,
                           "l2": "emptied before every launch", "clocks": clocks}
+    if not args.no_cpu_baseline:
+        out["route_sweep"]["cpu_baseline"] = cpu_leg(wl, {"logits": W.make_logits(wl, dev)},
+                                                     args.config_cpu_seconds)
     torch.cuda.empty_cache()
     for name, steps, fl in (("decode", max(50, args.steps), flush), ("prefill", args.steps, None),
                             ("tiny_f32", max(20, args.steps), None)):
@@ -727,6 +757,8 @@ def other_configs(moe, dev, args):
         if name == "tiny_f32":
             e["roofline"] = None
             e["note"] = "correctness workload (parity in tests/test_gpu_parity.py::test_layer_tiny_f32)"
+        if not args.no_cpu_baseline:
+            e["cpu_baseline"] = cpu_leg(wl, m["inputs"], args.config_cpu_seconds)
         out[name] = e
         del m
         torch.cuda.empty_cache()
