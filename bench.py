@@ -512,7 +512,7 @@ def run_sigmoid(args):
             "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E,
                        "top_k": wl.top_k, "groups": G, "selected_groups": SG,
                        "group_top_two": True, "l2": "emptied before each router launch (256 MB written, then 256 MB read)"},
-            "roofline": {"kernel": "moe_route_sigmoid_kernel (float64 selection, warp per row)",
+            "roofline": {"kernel": "moe_route_sigmoid_sub (sub-warp rows; FP32 decision, float64 only where a margin fails)",
                          "bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / pk["hbm_gbs"], "peak_source": f"{pk_src} HBM copy",
                          "traffic": None, "algorithmic_bytes_per_launch": nbytes},

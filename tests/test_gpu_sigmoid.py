@@ -55,11 +55,13 @@ def test_sigmoid_route_matches_oracle(dt, E, G, SG, k, top2, renorm, with_bias):
 
 
 @pytest.mark.parametrize("top2", [True, False])
-def test_sigmoid_route_near_ties(top2):
+@pytest.mark.parametrize("E,G,SG,k", [(64, 8, 3, 6), (256, 8, 4, 8)])
+def test_sigmoid_route_near_ties(top2, E, G, SG, k):
     """f32 logits a few ulps apart around a handful of values: most rows fall inside the FP32
-    error margin of the first pass and are decided in float64, the rest by the FP32 pass; the
-    indices must be the float64 decision either way."""
-    T, E, G, SG, k = 2000, 64, 8, 3, 6
+    error margin of the first pass and are decided in float64 (the runs of close candidates up to
+    the k-th, or the whole row), the rest by the FP32 pass; the indices must be the float64
+    decision either way."""
+    T = 2000
     g = torch.Generator().manual_seed(11)
     base = torch.tensor([-1.0, 0.25, 0.5, 1.75], dtype=torch.float32)[
         torch.randint(0, 4, (T, E), generator=g)]
@@ -105,3 +107,67 @@ def test_sigmoid_forward_matches_oracle(dt):
                                     True, True, 1.5)
     err = rel_max_err(f64(out), ref["out_unrounded"])
     assert err <= layer_tol(dt), err
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("E,G,SG,k", [(256, 8, 4, 8), (64, 8, 3, 6), (256, 8, 1, 8)])
+@pytest.mark.parametrize("with_bias", [True, False])
+def test_sigmoid_route_crowded_rows(dt, E, G, SG, k, with_bias):
+    """Rows whose chosen groups hold many candidates at or near the k-th score: constant rows (every
+    candidate ties), rows of a few repeated values (dozens of exact ties at the line), and rows with
+    one dominant value per group.  They exercise both forms of the top-k inside the chosen groups:
+    the ranked compaction of the candidates near the line, and the rounds of sub-warp argmax when
+    more candidates sit there than the compaction holds."""
+    T = 480
+    g = torch.Generator().manual_seed(E + SG + k)
+    l = torch.randn(T, E, generator=g)
+    l[0:60] = 0.5                                                      # constant rows
+    l[60:120] = 0.0
+    l[120:240] = torch.randint(0, 3, (120, E), generator=g).float()   # three values
+    l[240:300] = torch.randint(0, 2, (60, E), generator=g).float() * 4 - 2
+    l[300:360, ::5] = 3.0                                              # a dominant value
+    l = l.to(dt)
+    bias = None
+    if with_bias:
+        bias = torch.zeros(E)
+        bias[::7] = 0.25                                               # lifts a few experts
+    idx, w = moe.moe_route_sigmoid_grouped(l.to(DEV), k, G, SG, True, True, 1.0,
+                                           None if bias is None else bias.to(DEV))
+    torch.cuda.synchronize()
+    arr, name = storage(l)
+    b64 = None if bias is None else bias.double().numpy()
+    ridx, rw = O.route_sigmoid_grouped(O.to_f64(arr, name), b64, k, G, SG, True, True, 1.0, name)
+    np.testing.assert_array_equal(u32(idx), ridx)
+    check_weights(w, rw, f"sigmoid crowded {name} E={E} SG={SG}")
+
+
+@pytest.mark.parametrize("E,G,SG,k", [(256, 8, 4, 8), (64, 8, 3, 6)])
+def test_sigmoid_route_close_pairs(E, G, SG, k):
+    """Rows with a few candidates one or two ulps apart at chosen places of the ranking (inside the
+    top k, across the k-th / (k+1)-th boundary, a chain of four), the rest well apart: the FP32
+    pass proves all but the close runs, which are ordered by their float64 scores."""
+    T = 1000
+    g = torch.Generator().manual_seed(E + k)
+    l = torch.randn(T, E, generator=g) * 2
+    order = l.argsort(dim=1, descending=True)
+    rows = torch.arange(T)
+
+    def tie(r, p, q, ulps):  # logit at sorted place q := logit at place p moved by `ulps` ulps
+        src = l[r, order[r, p]]
+        moved = (src.view(torch.int32) + torch.tensor(ulps, dtype=torch.int32)).view(torch.float32)
+        l[r, order[r, q]] = moved
+
+    for r in range(0, 250):
+        tie(r, 2, 3, -1)
+    for r in range(250, 500):
+        tie(r, k - 1, k, 1 if r % 2 else -1)
+    for r in range(500, 750):
+        for q in range(k - 3, k + 1):
+            tie(r, k - 4, q, -(q - k + 4) * (1 if r % 3 else -1))
+    assert rows.numel() == T
+    idx, w = moe.moe_route_sigmoid_grouped(l.to(DEV), k, G, SG, True, True, 1.0, None)
+    torch.cuda.synchronize()
+    ridx, rw = O.route_sigmoid_grouped(O.to_f64(*storage(l)), None, k, G, SG, True, True, 1.0,
+                                       "f32")
+    np.testing.assert_array_equal(u32(idx), ridx)
+    check_weights(w, rw, "sigmoid close pairs")
