@@ -344,6 +344,13 @@ def _run_layer(wl, sample=None, seed=0):
     np.testing.assert_array_equal(d["offsets"].cpu().numpy(), offsets)
     np.testing.assert_array_equal(u32(d["row_of_slot"]), r_of_s)
     np.testing.assert_array_equal(u32(d["token_of_row"]), t_of_r)
+    # moe_forward runs the same kernels as the staged calls: bit for bit the same output
+    y = moe.moe_experts_forward_dispatched(d["x_d"], d["offsets"], g["gate"], g["up"], g["down"])
+    out_st = moe.moe_combine(y, d["row_of_slot"], w)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.uint8), out_st.view(torch.uint8)), \
+        f"{wl.name}: moe_forward differs from the staged calls"
+    del y, out_st
     wname = DT_NAME[g["x"].dtype]
     if sample == "stratified":
         tok = _stratified_tokens(offsets, t_of_r, wl.T, 2048, seed)
@@ -374,6 +381,21 @@ def test_layer_tiny_f32():
 def test_layer_small_bf16_full_oracle():
     _run_layer(W.Workload("small_bf16", T=300, H=256, I=512, E=16, top_k=4, renormalize=False,
                           dtype="bf16", seed=21, zipf_s=1.0))
+
+
+@pytest.mark.parametrize("wl", [
+    # CTA-pair experts (at least 128 rows an expert on average) at sizes the oracle runs whole:
+    # even experts; ragged experts with idle ones, H = 200 (a K tail) and I = 192 (an N tail);
+    # f16 with top_k = 3
+    W.Workload("pair_even", T=700, H=256, I=256, E=4, top_k=2, renormalize=True, dtype="bf16",
+               seed=41),
+    W.Workload("pair_ragged", T=1100, H=200, I=192, E=16, top_k=2, renormalize=False,
+               dtype="bf16", seed=42, zipf_s=1.3),
+    W.Workload("pair_f16", T=900, H=320, I=384, E=8, top_k=3, renormalize=True, dtype="f16",
+               seed=43, zipf_s=0.7),
+], ids=lambda w: w.name)
+def test_layer_pair_full_oracle(wl):
+    _run_layer(wl)
 
 
 def test_layer_decode_full():
