@@ -185,3 +185,50 @@ def test_full_backward_chain_matches_oracle(dt):
     assert rel_max_err(f64(dl), rdl) <= tol
     for got, ref in ((dg, rdg), (du, rdu), (dd, rdd)):
         assert rel_max_err(f64(got), ref) <= tol
+
+
+@pytest.mark.parametrize("counts,H,I", [
+    ([0, 300, 0, 0, 5, 64, 0, 1], 256, 128),        # tensor cores: idle experts between others
+    ([0, 0, 0, 0], 128, 64),                          # no rows at all: every gradient is zero
+    ([700, 0, 3, 0, 0, 600], 192, 256),               # CTA pairs for dA, g/u, dinput
+])
+def test_experts_backward_writes_every_gradient(counts, H, I):
+    """Through the C ABI with dinput and the FP32 weight-gradient buffers filled with NaN: the
+    library writes every element, the zero gradients of experts without rows included, and the
+    rest equals moe_experts_backward's result."""
+    from mixture_experts_routing_moe_gb300 import binding as B
+    dt = torch.bfloat16
+    E = len(counts)
+    _, offsets, _, _ = O.dispatch(_groups(counts, 5), E) if sum(counts) else (
+        None, np.zeros(E + 1, np.int64), None, None)
+    rows = int(offsets[-1])
+    g = torch.Generator().manual_seed(E + H + I)
+    x_d = torch.randn(max(rows, 1), H, generator=g).to(dt).to(DEV)[:rows]
+    gate = (torch.randn(E, I, H, generator=g) / H ** 0.5).to(dt).to(DEV)
+    up = (torch.randn(E, I, H, generator=g) / H ** 0.5).to(dt).to(DEV)
+    down = (torch.randn(E, H, I, generator=g) / I ** 0.5).to(dt).to(DEV)
+    dy = torch.randn(max(rows, 1), H, generator=g).to(dt).to(DEV)[:rows]
+    off_t = torch.from_numpy(offsets.astype(np.int32)).to(DEV)
+    nan = float("nan")
+    dx = torch.full((max(rows, 1), H), nan, dtype=dt, device=DEV)
+    dg = torch.full((E, I, H), nan, dtype=torch.float32, device=DEV)
+    du = torch.full((E, I, H), nan, dtype=torch.float32, device=DEV)
+    dd = torch.full((E, H, I), nan, dtype=torch.float32, device=DEV)
+    ws = torch.empty(max(B.lib().moe_experts_backward_workspace_bytes(rows, I), 256),
+                     dtype=torch.uint8, device=DEV)
+    st = B.lib().moe_experts_backward(
+        x_d.data_ptr(), off_t.data_ptr(), rows, gate.data_ptr(), up.data_ptr(), down.data_ptr(),
+        B.DTYPE_CODE[dt], E, H, I, dy.data_ptr(), dx.data_ptr(), dg.data_ptr(), du.data_ptr(),
+        dd.data_ptr(), ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    for name, t in (("dgate", dg), ("dup", du), ("ddown", dd), ("dinput", dx[:rows])):
+        assert not torch.isnan(t).any(), f"{name}: elements left unwritten"
+    idle = [e for e, n in enumerate(counts) if n == 0]
+    for t in (dg, du, dd):
+        assert torch.count_nonzero(t[idle]) == 0
+    if rows:
+        rx, rg, ru, rd = moe.moe_experts_backward(x_d, off_t, gate, up, down, dy)
+        torch.cuda.synchronize()
+        for got, ref in ((dx[:rows], rx), (dg, rg), (du, ru), (dd, rd)):
+            assert torch.equal(got, ref)
