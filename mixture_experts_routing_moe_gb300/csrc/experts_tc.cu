@@ -110,7 +110,7 @@ constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;
 // down epilogue: one 32-row x 64-column bf16 staging buffer (4 KB) per epilogue warp
 constexpr int kStage2Out = 32 * 128;
 constexpr size_t kSmem2Bytes = 1024 + (size_t)STAGES2 * STAGE2_BYTES + 256 +
-                               (kMaxExperts + 4) * sizeof(int) + 4 * kStage2Out;
+                               2 * (kMaxExperts + 4) * sizeof(int) + 4 * kStage2Out;
 
 // The GEMMs the pair kernel runs.  Forward: gate/up (A = x_d, B = interleaved gate / up halves,
 // a = silu(g) u) and down (A = a, B = down, plain cast).  Expert backward (ruDNN user guide §12):
@@ -148,9 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 5);
   volatile int* abort_f = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* pref = reinterpret_cast<int*>(tmem_slot + 4);
-  // staging of the down epilogue, after the barriers (256 B) and the prefix (kMaxExperts + 4 ints)
+  int* offs = pref + (kMaxExperts + 4);  // a copy of offsets[0 .. E]
+  // staging of the down epilogue, after the barriers (256 B), the prefix and the offsets
   const uint32_t stage_out =
-      base + STAGES2 * STAGE2_BYTES + 256 + (uint32_t)((kMaxExperts + 4) * sizeof(int));
+      base + STAGES2 * STAGE2_BYTES + 256 + (uint32_t)(2 * (kMaxExperts + 4) * sizeof(int));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -171,6 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) tmem_alloc2(smem_u32(tmem_slot), kTmemCols);
   if (warp == 2) build_mtile_prefix(p.offsets, p.E, BM2, pref, lane);
+  if (warp == 3)
+    for (int i = lane; i <= p.E; i += 32) offs[i] = __ldg(p.offsets + i);
   if (warp == 0 && lane == 0) {
     tma_prefetch(&mapA);
     tma_prefetch(&mapB0);
@@ -190,12 +193,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool stop = false;
       const uint64_t keep = policy_evict_last(), other = policy_evict_normal();
+      TileCursor<BM2> cur(pref, p.E, p.NT, p.KB * BK);
       for (int t = pair; t < total && !stop; t += npairs) {
         int e, m, n;
-        const bool a_res = decode_tile<BM2>(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
+        const bool a_res = cur.next(t, e, m, n);
         const uint64_t pa = a_res ? keep : other, pb = a_res ? other : keep;
-        const int r0 = __ldg(p.offsets + e) + m * BM2;
-        const bool half = __ldg(p.offsets + e + 1) - r0 <= 128;
+        const int r0 = offs[e] + m * BM2;
+        const bool half = offs[e + 1] - r0 <= 128;
         const int a_row = r0 + (int)rank * (half ? 64 : 128);
         const int b_row = GATEUP ? e * p.b_rows + n * (BN / 2) + (int)rank * 64
                                  : e * p.b_rows + n * BN + (int)rank * 128;
@@ -256,11 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool stop = false;
+      TileCursor<BM2> cur(pref, p.E, p.NT, p.KB * BK);
       for (int t = pair; t < total && !stop; t += npairs) {
         int e, m, n;
-        decode_tile<BM2>(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
-        const int r0 = __ldg(p.offsets + e) + m * BM2;
-        const uint32_t idesc = __ldg(p.offsets + e + 1) - r0 <= 128 ? idesc_half : idesc_full;
+        cur.next(t, e, m, n);
+        const int r0 = offs[e] + m * BM2;
+        const uint32_t idesc = offs[e + 1] - r0 <= 128 ? idesc_half : idesc_full;
         if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_f, p.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
@@ -295,14 +300,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
+    TileCursor<BM2> cur(pref, p.E, p.NT, p.KB * BK);
     for (int t = pair; t < total; t += npairs) {
       int e, m, n;
-      decode_tile<BM2>(t, pref, p.E, p.NT, p.KB * BK, e, m, n);
+      cur.next(t, e, m, n);
       const bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_f, p.status);
       if (!__all_sync(0xFFFFFFFFu, ok)) break;
       tc_fence_after();
-      const int r0 = __ldg(p.offsets + e) + m * BM2;
-      const int r_end = __ldg(p.offsets + e + 1);
+      const int r0 = offs[e] + m * BM2;
+      const int r_end = offs[e + 1];
       const bool half = r_end - r0 <= 128;
       // full tile: lane quarter q holds rows 128 rank + 32 q + lane over all N columns;
       // half tile: quarters 0-1 hold rows 64 rank + 32 q + lane for N columns 0-127, quarters 2-3

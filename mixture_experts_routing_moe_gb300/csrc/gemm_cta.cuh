@@ -65,6 +65,45 @@ __device__ __forceinline__ bool decode_tile(int t, const int* pref, int E, int N
   return false;
 }
 
+// The same decoding for one role's tiles, visited in increasing t (t, t + P, ...): the expert is
+// found by scanning forward from the previous tile's (no binary search), and the L2 residency
+// groups are sized once per launch, so the MMA issuer's step from one tile to the next is short.
+template <int TBM>
+struct TileCursor {
+  const int* pref;
+  int E, NT, fit_m, fit_n;  // m-tiles / n-tiles whose K-deep rows fit kResidentBytes
+  int e;
+  __device__ TileCursor(const int* pref_, int E_, int NT_, int K) : pref(pref_), E(E_), NT(NT_), e(0) {
+    const long long rows_fit = kResidentBytes / ((long long)K * 2);
+    fit_m = (int)max(1ll, min(rows_fit / TBM, 1ll << 30));
+    fit_n = (int)max(1ll, min(rows_fit / BN, 1ll << 30));
+  }
+  // t -> (e, m, n) as decode_tile<TBM>; returns true when A is the resident operand.
+  __device__ __forceinline__ bool next(int t, int& e_out, int& m, int& n) {
+    const int j = t / NT;  // the tile's global m-tile
+    while (e + 1 < E && pref[e + 1] <= j) ++e;
+    e_out = e;
+    const int local = t - pref[e] * NT;
+    const int mt = pref[e + 1] - pref[e];
+    if ((long long)mt * TBM <= (long long)NT * BN) {
+      const int g = min(mt, fit_m);
+      const int grp = local / (g * NT);
+      const int gm = min(g, mt - grp * g);
+      const int r = local - grp * g * NT;
+      n = r / gm;
+      m = grp * g + (r - n * gm);
+      return true;
+    }
+    const int g = min(NT, fit_n);
+    const int grp = local / (g * mt);
+    const int gn = min(g, NT - grp * g);
+    const int r = local - grp * g * mt;
+    m = r / gn;
+    n = grp * g + (r - m * gn);
+    return false;
+  }
+};
+
 struct TcParams {
   const int32_t* offsets;  // [E + 1] in global memory, or in shared memory when FUSED
   uint8_t* out;            // a [rows, N] (gate/up) or y [rows, N] (down), 16-bit elements
