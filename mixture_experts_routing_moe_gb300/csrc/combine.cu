@@ -23,7 +23,7 @@ __global__ void __launch_bounds__(kCombWarps * 32)
   const int64_t gw = (int64_t)blockIdx.x * kCombWarps + (threadIdx.x >> 5);
   const int64_t t = gw / warps_per_token;
   if (t >= T) return;
-  combine_warp<TY, TW, VEC, false, 1>(y, row_of_slot, w, t, H, k, gw - t * warps_per_token, out,
+  combine_warp<TY, TW, VEC, false, 2>(y, row_of_slot, w, t, H, k, gw - t * warps_per_token, out,
                                       lane);
 }
 

@@ -11,7 +11,8 @@
 namespace moe {
 
 // BATCH: slots whose loads are issued before their FMAs (8 where few warps are in flight, as in
-// the fused kernel; 1 where many warps already hide the load latency).
+// the fused kernel; 2 in the stage kernel, whose many warps hide most of the load latency: on the
+// skewed layer 2 measured 3 % faster than 1, 4 and 8 slower).
 template <typename TY, typename TW, bool VEC, bool COHERENT, int BATCH>
 __device__ __forceinline__ void combine_warp(const TY* __restrict__ y,
                                              const uint32_t* __restrict__ row_of_slot,
