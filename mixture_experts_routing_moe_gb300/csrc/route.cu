@@ -256,10 +256,12 @@ __device__ __forceinline__ void exact_row(const uint4* rowv, int sw, float x0, i
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       // monotone code of both halves: negative -> all bits flipped, else sign bit set; prmt
-      // with selector 0xBB99 replicates each half's sign bit over the half
+      // with selector 0xBB99 replicates each half's sign bit over the half.  A -0 half is
+      // first made +0 (equal logits share a code, and the lower id goes first).
+      const uint32_t wz = w[i] & ~__vcmpeq2(w[i], 0x80008000u);
       uint32_t sm;
-      asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(sm) : "r"(w[i]));
-      const uint32_t m = w[i] ^ (sm | 0x80008000u);
+      asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(sm) : "r"(wz));
+      const uint32_t m = wz ^ (sm | 0x80008000u);
       const uint32_t e0 = v * 8 + i * 2;
       g[2 * i] = (m << 16) | (0xFFFFu - e0);
       g[2 * i + 1] = (m & 0xFFFF0000u) | (0xFFFFu - (e0 + 1));

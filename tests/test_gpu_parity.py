@@ -123,6 +123,33 @@ def test_route_half_width_boundary(dt, k, renorm):
     check_weights(w, rw, f"half-width boundary {name} k={k}")
 
 
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("E,k", [(8, 3), (64, 4), (64, 8), (256, 8), (40, 5)])
+def test_route_signed_zero_ties(dt, E, k):
+    """+0 and -0 are equal logits: where they meet at the top-k boundary the lower id goes first,
+    whatever the signs.  Rows hold six zeros of both signs at random places among negative logits
+    (some of them ties at -1), and rows whose largest values are -0 only."""
+    g = torch.Generator().manual_seed(E + k)
+    rows = []
+    for i in range(120):
+        r = -1.0 - torch.randint(0, 3, (E,), generator=g).float()
+        pos = torch.randperm(E, generator=g)[:min(6, E)]
+        signs = torch.randint(0, 2, (len(pos),), generator=g)
+        if i % 4 == 0:
+            signs[:] = 1                                          # -0 only
+        r[pos] = torch.where(signs == 1, torch.tensor(-0.0), torch.tensor(0.0))
+        rows.append(r)
+    l = torch.stack(rows).to(dt)
+    assert (torch.signbit(l.float()) & (l.float() == 0)).any()
+    for renorm in (True, False):
+        idx, w = moe.moe_route(l.to(DEV), k, renorm)
+        torch.cuda.synchronize()
+        arr, name = storage(l)
+        ridx, rw = O.route(O.to_f64(arr, name), k, renorm, name)
+        np.testing.assert_array_equal(u32(idx), ridx)
+        check_weights(w, rw, f"signed zeros {name} E={E} k={k}")
+
+
 @pytest.mark.parametrize("dt,scales", [(torch.bfloat16, [300.0, -300.0, 1e6, 1e20, 1e30, -1e30]),
                                        (torch.float16, [300.0, -300.0, 3e4, -3e4])])
 @pytest.mark.parametrize("E,k", [(64, 8), (40, 5), (128, 8)])
