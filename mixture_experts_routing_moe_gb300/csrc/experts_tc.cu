@@ -100,6 +100,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // columns 128-255, in TMEM columns 0-127 (layout measured on GB300).  This keeps the padding of
 // ragged experts at 128-row granularity; such a tile's CTAs load 64 A rows each (a 64-row map).  With half of B per CTA a stage is 32 KB, so six stages fit, and each CTA pulls a
 // third fewer bytes per FLOP through L2 than a single-CTA 128 x 256 tile.
+// Each role walks its tiles (pair, pair + P, ...) with a TileCursor over a shared-memory copy of
+// the offsets, so the MMA issuer's step from one tile to the next holds no global load, binary
+// search or 64-bit division while the tensor pipe drains.
 // Synchronisation: both CTAs' TMA loads signal CTA 0's full barrier (CTA 0 arms it for both);
 // CTA 0's MMA commits are multicast to the empty / tmem-full barriers of both CTAs; all eight
 // epilogue warps arrive on CTA 0's tmem-empty barrier.  Waits are bounded as in the CTA kernel.
