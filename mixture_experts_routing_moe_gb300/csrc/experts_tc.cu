@@ -100,9 +100,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 // columns 128-255, in TMEM columns 0-127 (layout measured on GB300).  This keeps the padding of
 // ragged experts at 128-row granularity; such a tile's CTAs load 64 A rows each (a 64-row map).  With half of B per CTA a stage is 32 KB, so six stages fit, and each CTA pulls a
 // third fewer bytes per FLOP through L2 than a single-CTA 128 x 256 tile.
-// Each role walks its tiles (pair, pair + P, ...) with a TileCursor over a shared-memory copy of
-// the offsets, so the MMA issuer's step from one tile to the next holds no global load, binary
-// search or 64-bit division while the tensor pipe drains.
+// Tiles are claimed dynamically: a pair's first tile is tile `pair`; CTA 0's producer claims each
+// later one from a global counter and writes its id into a 4-slot ring in both CTAs (full / empty
+// mbarriers; the id reaches CTA 1 by a cluster store ordered by a release arrive), and every role
+// of both CTAs reads the ids in order, so pairs that finish early take the last tiles instead of a
+// static share.  Each role walks its (increasing) tiles with a TileCursor over a shared-memory
+// copy of the offsets, so the MMA issuer's step from one tile to the next holds no global load,
+// binary search or 64-bit division while the tensor pipe drains.
 // Synchronisation: both CTAs' TMA loads signal CTA 0's full barrier (CTA 0 arms it for both);
 // CTA 0's MMA commits are multicast to the empty / tmem-full barriers of both CTAs; all eight
 // epilogue warps arrive on CTA 0's tmem-empty barrier.  Waits are bounded as in the CTA kernel.
@@ -128,6 +132,38 @@ constexpr size_t kSmem2Bytes = 1024 + (size_t)STAGES2 * STAGE2_BYTES + 256 +
 // MN-major 128-byte-swizzled matrix (boxes 8 KB apart).
 enum PairKind { kGateUp = 0, kDown = 1, kDa = 2, kGu = 3, kDin = 4 };
 
+// Tile-id ring of the pair kernel (dynamic claims): slot q holds the id CTA 0's producer claimed.
+constexpr int kRing = 4;
+// 32-bit store into the shared memory of another CTA of the cluster (address from mapa).
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// try_wait with acquire at cluster scope: the phase was completed by another CTA's release.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool wait_bounded_cl(uint32_t bar, uint32_t parity,
+                                                volatile int* abort_f, unsigned* status) {
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    if (*abort_f) return false;
+    if (clock64() - t0 > kWaitLimit) {
+      *abort_f = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 template <int KIND, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_experts_tc2(const __grid_constant__ CUtensorMap mapA,
@@ -148,9 +184,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES2 + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES2 + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES2 + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 5);
+  auto rfull = [&](int q) { return bar0 + 8u * (2 * STAGES2 + 5 + q); };   // each CTA
+  auto rempty = [&](int q) { return bar0 + 8u * (2 * STAGES2 + 9 + q); };  // CTA 0's
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 13);
   volatile int* abort_f = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* pref = reinterpret_cast<int*>(tmem_slot + 4);
+  volatile int* rids = reinterpret_cast<volatile int*>(tmem_slot + 2);  // kRing tile ids
+  int* pref = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + 256);
   int* offs = pref + (kMaxExperts + 4);  // a copy of offsets[0 .. E]
   // staging of the down epilogue, after the barriers (256 B), the prefix and the offsets
   const uint32_t stage_out =
@@ -170,6 +209,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(tempty_bar(a), 8);
     }
     mbar_init(drain_bar, 1);
+    for (int q = 0; q < kRing; ++q) {
+      mbar_init(rfull(q), 1);
+      // readers of every id: CTA 0's MMA thread and epilogue warps, CTA 1's producer and
+      // epilogue warps
+      mbar_init(rempty(q), 10);
+    }
     *abort_f = 0;
     fence_mbar_init();
   }
@@ -188,6 +233,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int total = pref[p.E] * p.NT;
+  // Tile order.  Dynamic (p.tile_ctr set): a pair's first tile is tile `pair`, later ones are
+  // claimed from the global counter by CTA 0's producer, which writes each id into both CTAs'
+  // rings; every role of both CTAs reads the ids in order (so the pairs that finish early take
+  // the last tiles).  Static: pair, pair + P, ...  Either way a role's tiles increase.
+  const bool dyn = p.tile_ctr != nullptr;
+  int rq = 0, st_t = -1;
+  uint32_t rph = 0;
+  auto claim = [&]() -> int {  // CTA 0's producer: the next tile, published to both CTAs
+    if (!dyn) {
+      st_t = st_t < 0 ? pair : st_t + npairs;
+      return st_t < total ? st_t : -1;
+    }
+    if (!wait_bounded(rempty(rq), rph ^ 1u, abort_f, p.status)) return -2;
+    int t = st_t < 0 ? pair : npairs + (int)atomicAdd(p.tile_ctr, 1u);
+    st_t = t;
+    if (t >= total) t = -1;
+    rids[rq] = t;
+    st_cluster_u32(map_to_rank(smem_u32((const void*)(rids + rq)), 1), (uint32_t)t);
+    mbar_arrive(rfull(rq));
+    mbar_arrive_cluster(map_to_rank(rfull(rq), 1));  // release: the store above lands first
+    if (++rq == kRing) {
+      rq = 0;
+      rph ^= 1u;
+    }
+    return t;
+  };
+  // Every other role (one thread each: the producer of CTA 1, the MMA thread, lane 0 of each
+  // epilogue warp): the next id (-1: none left, -2: a wait gave up).
+  auto consume = [&](bool arrive) -> int {
+    if (!dyn) {
+      st_t = st_t < 0 ? pair : st_t + npairs;
+      return st_t < total ? st_t : -1;
+    }
+    const bool ok = leader ? wait_bounded(rfull(rq), rph, abort_f, p.status)
+                           : wait_bounded_cl(rfull(rq), rph, abort_f, p.status);
+    if (!ok) return -2;
+    const int t = rids[rq];
+    if (arrive) {
+      if (leader) mbar_arrive(rempty(rq));
+      else mbar_arrive_cluster(map_to_rank(rempty(rq), 0));
+    }
+    if (++rq == kRing) {
+      rq = 0;
+      rph ^= 1u;
+    }
+    return t;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -197,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool stop = false;
       const uint64_t keep = policy_evict_last(), other = policy_evict_normal();
       TileCursor<BM2> cur(pref, p.E, p.NT, p.KB * BK);
-      for (int t = pair; t < total && !stop; t += npairs) {
+      for (int t = leader ? claim() : consume(true); t >= 0 && !stop;
+           t = leader ? claim() : consume(true)) {
         int e, m, n;
         const bool a_res = cur.next(t, e, m, n);
         const uint64_t pa = a_res ? keep : other, pb = a_res ? other : keep;
@@ -264,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, acc_phase = 0;
       bool stop = false;
       TileCursor<BM2> cur(pref, p.E, p.NT, p.KB * BK);
-      for (int t = pair; t < total && !stop; t += npairs) {
+      for (int t = consume(true); t >= 0 && !stop; t = consume(true)) {
         int e, m, n;
         cur.next(t, e, m, n);
         const int r0 = offs[e] + m * BM2;
@@ -304,7 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     TileCursor<BM2> cur(pref, p.E, p.NT, p.KB * BK);
-    for (int t = pair; t < total; t += npairs) {
+    while (true) {
+      int t = 0;
+      if (lane == 0) t = consume(true);  // one reader per warp; the id goes to every lane
+      t = __shfl_sync(0xFFFFFFFFu, t, 0);
+      if (t < 0) break;
       int e, m, n;
       cur.next(t, e, m, n);
       const bool ok = wait_bounded(tfull_bar(acc), acc_phase, abort_f, p.status);
@@ -573,6 +670,8 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUten
   const int64_t upper = ((rows + BM2 - 1) / BM2 + p.E) * (int64_t)p.NT;  // >= number of tiles
   const int pairs = (int)(upper < mp ? upper : mp);
   cfg.gridDim = dim3(2 * pairs);
+  if (p.tile_ctr && (err = cudaMemsetAsync(p.tile_ctr, 0, sizeof(unsigned), s)) != cudaSuccess)
+    return err;
   return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, ah, p);
 }
 
@@ -595,7 +694,10 @@ cudaError_t launch_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, c
       !make_map(&md, down, BF16, I, (int64_t)E * H, pair ? BN / 2 : BN))
     return cudaErrorInvalidValue;
 
+  // the pair kernels' tile-claim counter: byte 192 of the caller's 256-byte workspace header
+  unsigned* tile_ctr = status ? status + 48 : nullptr;
   TcParams p1{offsets, (uint8_t*)a, status, E, I, (H + BK - 1) / BK, (I + BN / 2 - 1) / (BN / 2), I};
+  p1.tile_ctr = tile_ctr;
   CUtensorMap mxh, mah;  // the pair kernel's half tiles load 64 rows of x_d / a per CTA
   if (pair) {  // the pair kernel loads gate and up in 64-row boxes (interleaved B halves)
     if (!make_map(&mg, gate, BF16, H, (int64_t)E * I, BN / 4) ||
@@ -608,6 +710,7 @@ cudaError_t launch_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, c
   if (err != cudaSuccess) return err;
   if (between && (err = cudaEventRecord(between, s)) != cudaSuccess) return err;
   TcParams p2{offsets, (uint8_t*)y, status, E, H, (I + BK - 1) / BK, (H + BN - 1) / BN, H};
+  p2.tile_ctr = tile_ctr;
   return pair ? launch_pair<kDown, BF16>(ma, md, md, mah, p2, rows, dev, s)
               : launch_one<false, BF16>(ma, md, md, p2, rows, sms, s);
 }
@@ -625,7 +728,9 @@ cudaError_t bwd_pair_t(const void* x_d, const int32_t* offsets, int64_t rows, co
   if (!make_map(&mA, dy, BF16, H, rows, BM) || !make_map(&mAh, dy, BF16, H, rows, BM / 2) ||
       !tc::make_map_2d(&mB0, down, BF16, I, (int64_t)E * H, 64, 64))
     return cudaErrorInvalidValue;
+  unsigned* tile_ctr = status ? status + 48 : nullptr;  // byte 192 of the workspace header
   TcParams p1{offsets, (uint8_t*)da, status, E, I, (H + BK - 1) / BK, (I + BN - 1) / BN, H};
+  p1.tile_ctr = tile_ctr;
   err = launch_pair<kDa, BF16>(mA, mB0, mB0, mAh, p1, rows, dev, s);
   if (err != cudaSuccess) return err;
   // 2. g, u recomputed (gate and up in 64-row K-major boxes, as the forward), SwiGLU gradient
@@ -637,6 +742,7 @@ cudaError_t bwd_pair_t(const void* x_d, const int32_t* offsets, int64_t rows, co
   p2.da = da;
   p2.out1 = (uint8_t*)a;
   p2.I = I;
+  p2.tile_ctr = tile_ctr;
   err = launch_pair<kGu, BF16>(mA, mB0, mB1, mAh, p2, rows, dev, s);
   if (err != cudaSuccess) return err;
   // 3. dinput = [dg du] [gate_e; up_e]: gate and up read as [E I, H] (N = H contiguous)
@@ -647,6 +753,7 @@ cudaError_t bwd_pair_t(const void* x_d, const int32_t* offsets, int64_t rows, co
     return cudaErrorInvalidValue;
   TcParams p3{offsets, (uint8_t*)dinput, status, E, H, 2 * I / BK, (H + BN - 1) / BN, I};
   p3.I = I;
+  p3.tile_ctr = tile_ctr;
   return launch_pair<kDin, BF16>(mA, mB0, mB1, mAh, p3, rows, dev, s);
 }
 

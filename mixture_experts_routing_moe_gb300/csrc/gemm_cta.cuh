@@ -127,6 +127,9 @@ struct TcParams {
   const float* da;
   uint8_t* out1;
   int I;
+  // CTA-pair kernels: tiles after each pair's first are claimed from this counter (zero at launch;
+  // null: the static order pair, pair + P, ...)
+  unsigned* tile_ctr;
 };
 
 __device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
