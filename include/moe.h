@@ -19,6 +19,9 @@
  *  - Kernels never trap.  Conditions only the device can see (an expert index >= E handed to
  *    moe_dispatch; a pipeline wait in the tensor-core kernels that exceeded its time limit) are
  *    recorded in a status word at the start of the workspace; moe_device_status() reads it.
+ *    The workspace's first 256 bytes are the library's own (the status word and counters the
+ *    kernels of one call use, e.g. the tile-claim counter of the tensor-core grouped GEMMs); one
+ *    workspace therefore serves one call in flight at a time.
  *  - dtype codes: MOE_F32, MOE_F16, MOE_BF16 (unquantised, as §4 "Routing-Vertrag" requires).
  *  - Limits: 1 <= top_k <= E <= 1024; T * top_k < 2^31; H, I >= 1.
  */
