@@ -100,11 +100,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // columns 128-255, in TMEM columns 0-127 (layout measured on GB300).  This keeps the padding of
 // ragged experts at 128-row granularity; such a tile's CTAs load 64 A rows each (a 64-row map).  With half of B per CTA a stage is 32 KB, so six stages fit, and each CTA pulls a
 // third fewer bytes per FLOP through L2 than a single-CTA 128 x 256 tile.
-// Tiles are claimed dynamically: a pair's first tile is tile `pair`; CTA 0's producer claims each
-// later one from a global counter and writes its id into a 4-slot ring in both CTAs (full / empty
-// mbarriers; the id reaches CTA 1 by a cluster store ordered by a release arrive), and every role
-// of both CTAs reads the ids in order, so pairs that finish early take the last tiles instead of a
-// static share.  Each role walks its (increasing) tiles with a TileCursor over a shared-memory
+// GEMMs with long tiles (at least 96 K blocks) claim them dynamically: a pair's first tile is tile
+// `pair`; CTA 0's producer claims each later one from a global counter, one tile ahead, and writes
+// its id into an 8-slot ring in both CTAs (full / empty mbarriers; the id reaches CTA 1 by a
+// cluster store ordered by a release arrive), and every role of both CTAs reads the ids in order,
+// so pairs that finish early take the last tiles instead of a static share.  Short tiles keep the
+// static order pair, pair + P, ... (their boundaries would pay the hand-off more often).  Each role walks its (increasing) tiles with a TileCursor over a shared-memory
 // copy of the offsets, so the MMA issuer's step from one tile to the next holds no global load,
 // binary search or 64-bit division while the tensor pipe drains.
 // Synchronisation: both CTAs' TMA loads signal CTA 0's full barrier (CTA 0 arms it for both);
@@ -116,7 +117,8 @@ constexpr int B2_BYTES = 128 * BK * 2;  // 16 KB: half of the 256-row B tile
 constexpr int STAGE2_BYTES = A2_BYTES + B2_BYTES;
 // down epilogue: one 32-row x 64-column bf16 staging buffer (4 KB) per epilogue warp
 constexpr int kStage2Out = 32 * 128;
-constexpr size_t kSmem2Bytes = 1024 + (size_t)STAGES2 * STAGE2_BYTES + 256 +
+constexpr int kBar2Bytes = 512;  // mbarriers, TMEM slot, abort flag, tile-id ring
+constexpr size_t kSmem2Bytes = 1024 + (size_t)STAGES2 * STAGE2_BYTES + kBar2Bytes +
                                2 * (kMaxExperts + 4) * sizeof(int) + 4 * kStage2Out;
 
 // The GEMMs the pair kernel runs.  Forward: gate/up (A = x_d, B = interleaved gate / up halves,
@@ -133,7 +135,9 @@ constexpr size_t kSmem2Bytes = 1024 + (size_t)STAGES2 * STAGE2_BYTES + 256 +
 enum PairKind { kGateUp = 0, kDown = 1, kDa = 2, kGu = 3, kDin = 4 };
 
 // Tile-id ring of the pair kernel (dynamic claims): slot q holds the id CTA 0's producer claimed.
-constexpr int kRing = 4;
+constexpr int kRing = 8;
+// GEMMs with at least this many 64-deep K blocks a tile claim their tiles dynamically.
+constexpr int kDynamicMinKB = 96;
 // 32-bit store into the shared memory of another CTA of the cluster (address from mapa).
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
@@ -184,16 +188,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES2 + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES2 + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES2 + 4);
-  auto rfull = [&](int q) { return bar0 + 8u * (2 * STAGES2 + 5 + q); };   // each CTA
-  auto rempty = [&](int q) { return bar0 + 8u * (2 * STAGES2 + 9 + q); };  // CTA 0's
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 13);
+  auto rfull = [&](int q) { return bar0 + 8u * (2 * STAGES2 + 5 + q); };           // each CTA
+  auto rempty = [&](int q) { return bar0 + 8u * (2 * STAGES2 + 5 + kRing + q); };  // CTA 0's
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 5 + 2 * kRing);
   volatile int* abort_f = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* rids = reinterpret_cast<volatile int*>(tmem_slot + 2);  // kRing tile ids
-  int* pref = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + 256);
+  int* pref = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + kBar2Bytes);
   int* offs = pref + (kMaxExperts + 4);  // a copy of offsets[0 .. E]
-  // staging of the down epilogue, after the barriers (256 B), the prefix and the offsets
-  const uint32_t stage_out =
-      base + STAGES2 * STAGE2_BYTES + 256 + (uint32_t)(2 * (kMaxExperts + 4) * sizeof(int));
+  // staging of the down epilogue, after the barriers, the prefix and the offsets
+  const uint32_t stage_out = base + STAGES2 * STAGE2_BYTES + kBar2Bytes +
+                             (uint32_t)(2 * (kMaxExperts + 4) * sizeof(int));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -289,8 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool stop = false;
       const uint64_t keep = policy_evict_last(), other = policy_evict_normal();
       TileCursor<BM2> cur(pref, p.E, p.NT, p.KB * BK);
-      for (int t = leader ? claim() : consume(true); t >= 0 && !stop;
-           t = leader ? claim() : consume(true)) {
+      // CTA 0 claims and publishes the next tile before loading this one, so neither producer
+      // waits for a claim's round trip at a tile boundary
+      int t = leader ? claim() : consume(true);
+      while (t >= 0 && !stop) {
+        const int tn = leader ? claim() : 0;
         int e, m, n;
         const bool a_res = cur.next(t, e, m, n);
         const uint64_t pa = a_res ? keep : other, pb = a_res ? other : keep;
@@ -334,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             phase ^= 1u;
           }
         }
+        t = leader ? tn : consume(true);
       }
       if (*abort_f && leader) {  // let copies still in flight land before the pair exits
         for (int i = 0; i < min(armed, STAGES2); ++i) {
@@ -670,9 +678,13 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b0, const CUten
   const int64_t upper = ((rows + BM2 - 1) / BM2 + p.E) * (int64_t)p.NT;  // >= number of tiles
   const int pairs = (int)(upper < mp ? upper : mp);
   cfg.gridDim = dim3(2 * pairs);
-  if (p.tile_ctr && (err = cudaMemsetAsync(p.tile_ctr, 0, sizeof(unsigned), s)) != cudaSuccess)
+  // Dynamic tile claims pay where tiles are long (the tail they remove is about half a tile);
+  // short ones keep the static order, whose tile boundaries hold no hand-off.
+  TcParams q = p;
+  if (q.KB < kDynamicMinKB) q.tile_ctr = nullptr;
+  if (q.tile_ctr && (err = cudaMemsetAsync(q.tile_ctr, 0, sizeof(unsigned), s)) != cudaSuccess)
     return err;
-  return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, ah, p);
+  return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, ah, q);
 }
 
 template <bool BF16>
