@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // columns 128-255, in TMEM columns 0-127 (layout measured on GB300).  This keeps the padding of
 // ragged experts at 128-row granularity; such a tile's CTAs load 64 A rows each (a 64-row map).  With half of B per CTA a stage is 32 KB, so six stages fit, and each CTA pulls a
 // third fewer bytes per FLOP through L2 than a single-CTA 128 x 256 tile.
-// GEMMs with long tiles (at least 96 K blocks) claim them dynamically: a pair's first tile is tile
+// GEMMs with long tiles (at least 64 K blocks) claim them dynamically: a pair's first tile is tile
 // `pair`; CTA 0's producer claims each later one from a global counter, one tile ahead, and writes
 // its id into an 8-slot ring in both CTAs (full / empty mbarriers; the id reaches CTA 1 by a
 // cluster store ordered by a release arrive), and every role of both CTAs reads the ids in order,
@@ -137,7 +137,7 @@ enum PairKind { kGateUp = 0, kDown = 1, kDa = 2, kGu = 3, kDin = 4 };
 // Tile-id ring of the pair kernel (dynamic claims): slot q holds the id CTA 0's producer claimed.
 constexpr int kRing = 8;
 // GEMMs with at least this many 64-deep K blocks a tile claim their tiles dynamically.
-constexpr int kDynamicMinKB = 96;
+constexpr int kDynamicMinKB = 64;
 // 32-bit store into the shared memory of another CTA of the cluster (address from mapa).
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
