@@ -34,7 +34,11 @@ def _groups(counts, seed):
                                         # pairs (half tiles of 1, 129 and 44 rows, ragged
                                         # output columns, dinput's K crossing from gate to up)
                                         ([600, 0, 1, 257, 129, 256], 192, 256),
-                                        ([2000, 300], 512, 320)])
+                                        ([2000, 300], 512, 320),
+                                        # K of 64 slices: dA and g/u (H = 4096), dinput
+                                        # (2 I = 4096) on dynamic tile claims
+                                        ([400, 0, 129, 300], 4096, 128),
+                                        ([300, 200, 1], 128, 2048)])
 def test_experts_backward_matches_oracle(dt, counts, H, I):
     E = len(counts)
     _, offsets, _, _ = O.dispatch(_groups(counts, sum(counts)), E)

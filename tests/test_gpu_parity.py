@@ -330,6 +330,58 @@ def test_experts_match_oracle(dt, case):
     assert err <= layer_tol(dt), f"rel max err {err}"
 
 
+# K of at least 64 slices of 64 (H >= 4096 for gate/up, I >= 4096 for down) puts the CTA-pair
+# GEMMs on dynamic tile claims: each pair's first tile is its index, later ones come from a
+# global counter.  Few tiles (most pairs get none), one tile per pair, and more tiles than
+# co-resident pairs (claims past the first round).
+DYNAMIC_CASES = [
+    ([300, 1, 257, 0, 600], 4096, 128),          # gate/up: 8 tiles
+    ([700, 300, 2, 0], 256, 4096),                # down: 6 tiles, K = 4096
+    ([1500, 3, 0, 900, 129, 600], 4096, 1024),    # gate/up: 15 m-tiles x 8 n-tiles = 120 tiles
+]
+
+
+def _tile_rows(offsets, seed, per_tile=3):
+    """Rows of every 128-row m-tile of every expert: each tile's first and last row and a few
+    seeded others, so that a wrong tile order or a tile computed twice or not at all shows."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for e in range(len(offsets) - 1):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        for m in range(lo, hi, 128):
+            end = min(m + 128, hi)
+            out += [m, end - 1] + list(rng.integers(m, end, per_tile))
+    return np.unique(np.array(out, dtype=np.int64))
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("case", range(len(DYNAMIC_CASES)))
+def test_experts_dynamic_tile_claims(dt, case):
+    counts, H, I = DYNAMIC_CASES[case]
+    E = len(counts)
+    _, offsets, _, _ = O.dispatch(_rand_groups(counts, seed=40 + case), E)
+    rows = int(offsets[-1])
+    g = torch.Generator().manual_seed(400 + case)
+    x_d = torch.randn(rows, H, generator=g).to(dt)
+    gate = (torch.randn(E, I, H, generator=g) / H ** 0.5).to(dt)
+    up = (torch.randn(E, I, H, generator=g) / H ** 0.5).to(dt)
+    down = (torch.randn(E, H, I, generator=g) / I ** 0.5).to(dt)
+    off_t = torch.from_numpy(offsets.astype(np.int32)).to(DEV)
+    y = moe.moe_experts_forward_dispatched(x_d.to(DEV), off_t, gate.to(DEV), up.to(DEV),
+                                           down.to(DEV))
+    torch.cuda.synchronize()
+    # rows are independent: the oracle runs on the sampled rows with their experts' offsets
+    sel = _tile_rows(offsets, seed=case)
+    sub_off = np.searchsorted(sel, offsets, side="left")
+    name = DT_NAME[dt]
+    ref = O.experts(O.to_f64(*storage(x_d))[sel], sub_off, storage(gate)[0], storage(up)[0],
+                    storage(down)[0], name)
+    got = f64(y)[sel]
+    assert np.isfinite(got).all()
+    err = rel_max_err(got, ref)
+    assert err <= layer_tol(dt), f"rel max err {err}"
+
+
 # ------------------------------------------------------------------------------------ full layer
 def _stratified_tokens(offsets, token_of_row, T, n_total, seed):
     """A seeded token sample that puts at least one row in every 128-row m-tile of every expert's
