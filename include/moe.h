@@ -276,7 +276,11 @@ int moe_combine_backward(const void* y, int ydt, const uint32_t* row_of_slot, co
  * with FP32 accumulation: on tensor cores (tcgen05) for bf16/f16 with I % 64 == 0 and 16-byte
  * aligned operands, whose GEMM operands dy, dg, du and g s u are then rounded to `wdt` as the
  * forward rounds a; on CUDA cores with FP32 operands otherwise.  Experts without rows get zero
- * gradients.
+ * gradients.  On the tensor-core path those zeros are written beside the GEMMs on a second stream
+ * that the library keeps per device and context (created on the first call), forked from
+ * `stream` and joined back into it with two events created and released within the call, so
+ * every write is ordered before work enqueued on `stream` after the call.  While `stream` is
+ * being captured into a CUDA graph they are written on `stream` itself.
  * dy [rows, H] dtype wdt.  ws: moe_experts_backward_workspace_bytes(rows, I), 256-byte aligned.
  */
 size_t moe_experts_backward_workspace_bytes(int64_t rows, int64_t I);

@@ -214,7 +214,7 @@ DispatchPlan dispatch_plan(int64_t R) {
 // The id of the calling thread's current CUDA context (0 when none is current or the driver
 // entry points are unavailable).  Context ids are unique for the life of the process, so a
 // context that replaces a destroyed one (after cudaDeviceReset) never matches a cached id.
-static unsigned long long current_context_id() {
+unsigned long long current_context_id() {
   typedef CUresult (*GetCurrentFn)(CUcontext*);
   typedef CUresult (*GetIdFn)(CUcontext, unsigned long long*);
   static const std::pair<GetCurrentFn, GetIdFn> fns = []() {

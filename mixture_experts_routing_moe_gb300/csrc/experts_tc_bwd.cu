@@ -21,6 +21,7 @@
 // [E][M][N] map, so every store moves whole 128-byte lines and never crosses into the next
 // expert's slice.  All waits are bounded as in the forward.
 #include <atomic>
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -191,21 +192,129 @@ __global__ void __launch_bounds__(1024) moe_expert_order(const int32_t* __restri
   if (threadIdx.x == 0) order[E] = n_active;
 }
 
-// The weight gradients of experts without rows are zero: written here with 16-byte stores at the
-// HBM write rate, instead of as GEMM tiles.  Block (e, m, j) covers slice j of matrix m (dgate,
-// dup, ddown) of expert e; blocks of experts with rows return at once.
+// The weight gradients of experts without rows are zero: written here with 16-byte streaming
+// stores (evict-first in L2, so that the zeros do not push the GEMMs' operands out), instead of
+// as GEMM tiles.  Every block walks the idle experts and stores its grid-stride share of their
+// three matrices (dgate, dup, ddown) in batches of four stores a thread, so any grid size covers
+// them.  With window_ns > 0 the fill runs beside GEMMs that take about that long and use part
+// of HBM themselves: a burst of stores at the full write rate delays their operand loads by more
+// than it saves, so each block pauses after every batch, long enough to spread its share over
+// half the window (at most 2 us a batch; about 0.3 us of each batch goes to the stores).
 __global__ void __launch_bounds__(256)
-    moe_zero_idle_grads(const int32_t* __restrict__ offsets, float* __restrict__ g0,
-                        float* __restrict__ g1, float* __restrict__ g2, int64_t per_expert) {
-  const int e = blockIdx.x;
-  if (offsets[e + 1] > offsets[e]) return;
-  float* g = (blockIdx.y == 0 ? g0 : blockIdx.y == 1 ? g1 : g2) + (size_t)e * per_expert;
+    moe_zero_idle_grads(const int32_t* __restrict__ offsets, int E, float* __restrict__ g0,
+                        float* __restrict__ g1, float* __restrict__ g2, int64_t per_expert,
+                        int64_t window_ns) {
   const int64_t n4 = per_expert / 4;  // per_expert = I * H, a multiple of 64
-  float4* v = reinterpret_cast<float4*>(g);
-  for (int64_t i = (int64_t)blockIdx.z * blockDim.x + threadIdx.x; i < n4;
-       i += (int64_t)gridDim.z * blockDim.x)
-    v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  unsigned pause_ns = 0;
+  if (window_ns > 0) {
+    int idle = 0;
+    for (int e = 0; e < E; ++e) idle += offsets[e + 1] > offsets[e] ? 0 : 1;
+    const int64_t batches = ((int64_t)idle * 3 * n4 + 4 * stride - 1) / (4 * stride);
+    if (batches > 0) {
+      const int64_t p = window_ns / 2 / batches - 300;
+      pause_ns = p <= 0 ? 0u : p >= 2000 ? 2000u : (unsigned)p;
+    }
+  }
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int e = 0; e < E; ++e) {
+    if (offsets[e + 1] > offsets[e]) continue;
+#pragma unroll 1
+    for (int m = 0; m < 3; ++m) {
+      float4* v = reinterpret_cast<float4*>((m == 0 ? g0 : m == 1 ? g1 : g2) +
+                                            (size_t)e * per_expert);
+      for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += 4 * stride) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (i + u * stride < n4) __stcs(v + i + u * stride, z);
+        if (pause_ns) __nanosleep(pause_ns);
+      }
+    }
+  }
 }
+
+// The fill above, run beside the tensor-core GEMMs of steps 1-3 of the backward, which use about
+// half of HBM's bandwidth: on a second stream of this device's context (created on first use),
+// forked from the caller's stream before the first GEMM and joined back before the weight
+// gradients, with one block per SM, so that every SM keeps room for a GEMM CTA next to it (the
+// fill holds no shared memory and prefers the largest shared-memory carveout), paced over half
+// the GEMMs' time.  While the caller's stream is being captured into a graph the fill runs on
+// that stream itself, in order, at full width.
+class IdleGradFill {
+ public:
+  IdleGradFill(cudaStream_t s) : s_(s) {}
+  ~IdleGradFill() { join(); }
+  // Before the first GEMM is enqueued: the fill depends on nothing enqueued after this.
+  cudaError_t fork() {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s_, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+      return cudaSuccess;  // in order on s_
+    cudaError_t err = side_stream(&s2_);
+    if (err != cudaSuccess || !s2_) return err;
+    if ((err = cudaEventCreateWithFlags(&fork_, cudaEventDisableTiming)) != cudaSuccess ||
+        (err = cudaEventCreateWithFlags(&join_, cudaEventDisableTiming)) != cudaSuccess)
+      return err;
+    return cudaEventRecord(fork_, s_);
+  }
+  // After the first GEMM is enqueued, so that its CTAs are placed first.  window_ns: about how
+  // long the GEMMs beside the fill take.
+  cudaError_t launch(const int32_t* offsets, int E, float* g0, float* g1, float* g2,
+                     int64_t per_expert, int sms, int64_t window_ns) {
+    cudaError_t err = cudaFuncSetAttribute(moe_zero_idle_grads,
+                                           cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           (int)cudaSharedmemCarveoutMaxShared);
+    if (err != cudaSuccess) return err;
+    if (!fork_) {
+      moe_zero_idle_grads<<<4 * sms, 256, 0, s_>>>(offsets, E, g0, g1, g2, per_expert, 0);
+      return cudaGetLastError();
+    }
+    if ((err = cudaStreamWaitEvent(s2_, fork_, 0)) != cudaSuccess) return err;
+    moe_zero_idle_grads<<<sms, 256, 0, s2_>>>(offsets, E, g0, g1, g2, per_expert, window_ns);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    err = cudaEventRecord(join_, s2_);
+    if (err == cudaSuccess) recorded_ = true;
+    return err;
+  }
+  // The caller's stream waits for the fill (also on every early return, through the destructor).
+  cudaError_t join() {
+    cudaError_t err = cudaSuccess;
+    if (recorded_) err = cudaStreamWaitEvent(s_, join_, 0);
+    recorded_ = false;
+    if (fork_) cudaEventDestroy(fork_);
+    if (join_) cudaEventDestroy(join_);
+    fork_ = join_ = nullptr;
+    return err;
+  }
+
+ private:
+  // The second stream of the current device and context (null, and the fill in order, when
+  // the context cannot be identified).
+  static cudaError_t side_stream(cudaStream_t* out) {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static cudaStream_t st[kMaxDevices] = {};
+    static unsigned long long ctx_of[kMaxDevices] = {};
+    *out = nullptr;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    const unsigned long long ctx = current_context_id();
+    if (ctx == 0) return cudaSuccess;
+    if (!st[dev] || ctx != ctx_of[dev]) {  // a new context: the old stream went with the old one
+      cudaStream_t s2 = nullptr;
+      if ((err = cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking)) != cudaSuccess) return err;
+      st[dev] = s2;
+      ctx_of[dev] = ctx;
+    }
+    *out = st[dev];
+    return cudaSuccess;
+  }
+  cudaStream_t s_, s2_ = nullptr;
+  cudaEvent_t fork_ = nullptr, join_ = nullptr;
+  bool recorded_ = false;
+};
 
 // Pair tiles of an expert with n rows (modes other than WG).
 struct PairTiles {
@@ -621,6 +730,13 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
   p.I = I;
   p.status = status;
 
+  int sms = 0;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return err;
+  // the zero gradients of experts without rows, beside steps 1-3
+  IdleGradFill fill(s);
+  if ((err = fill.fork()) != cudaSuccess) return err;
+
   // 1-3 on CTA pairs (256-row tiles) when the experts average at least 128 rows, as the forward
   if (rows >= (int64_t)128 * E) {
     err = launch_experts_bwd_pair(x_d, offsets, rows, gate, up, down, BF16 ? MOE_BF16 : MOE_F16, E,
@@ -661,14 +777,16 @@ cudaError_t bwd_tc_t(const void* x_d, const int32_t* offsets, int64_t rows, cons
   err = launch_mode<DIN, BF16>(mA, mB0, mB1, mA, p, mt_upper * ((p.NT + 1) / 2), dev, s);
   if (err != cudaSuccess) return err;
   }
+  // steps 1-3: 10 R H I FLOPs, at about 1.4 PFLOP/s on the skewed layer's shapes
+  const int64_t window_ns = (int64_t)(10.0 * (double)rows * H * I / 1.4e6);
+  if ((err = fill.launch(offsets, E, dgate, dup, ddown, (int64_t)I * H, sms, window_ns)) !=
+          cudaSuccess ||
+      (err = fill.join()) != cudaSuccess)
+    return err;
 
-  // 4. weight gradients, contracted over each expert's rows, experts ordered by row count; the
-  // zero gradients of experts without rows by a fill
+  // 4. weight gradients of the experts with rows, contracted over each expert's rows, experts
+  // ordered by row count
   moe_expert_order<<<1, 1024, 0, s>>>(offsets, E, order);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  moe_zero_idle_grads<<<dim3((unsigned)E, 3, 32), 256, 0, s>>>(offsets, dgate, dup, ddown,
-                                                                (int64_t)I * H);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   p.order = order;

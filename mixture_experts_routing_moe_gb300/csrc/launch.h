@@ -66,6 +66,10 @@ cudaError_t launch_wait_selftest(unsigned* status, cudaStream_t s);
 // Device address of that scratch on the current device (looked up on first use per device).
 cudaError_t static_dispatch_scratch(void** ptr);
 
+// The id of the calling thread's current CUDA context, unique for the life of the process (0 when
+// none is current or the driver entry points are unavailable).
+unsigned long long current_context_id();
+
 cudaError_t launch_combine(const void* y, int ydt, const uint32_t* row_of_slot, const void* w,
                            int wdt, int64_t T, int64_t H, int k, void* out, cudaStream_t s);
 
