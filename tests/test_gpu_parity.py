@@ -57,6 +57,22 @@ def test_route_matches_oracle(dt, T, E, k, renorm):
     check_weights(w, rw, f"{name} T={T} E={E} k={k}")
 
 
+@pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("k,renorm", [(8, True), (8, False), (3, True)])
+def test_route_e64_streamed_tiles(dt, k, renorm):
+    """E = 64 at a size where 256-row tiles staged in shared memory run in several waves over
+    the SMs (T = 2 x 3 x 152 x 256 + 77 rows), with a ragged last tile (ties, NaN, inf and -inf
+    rows included)."""
+    T = 2 * 3 * 152 * 256 + 77
+    l = _logits(T, 64, dt, seed=6400 + k)
+    idx, w = moe.moe_route(l.to(DEV), k, renorm)
+    torch.cuda.synchronize()
+    arr, name = storage(l)
+    ridx, rw = O.route(O.to_f64(arr, name), k, renorm, name)
+    np.testing.assert_array_equal(u32(idx), ridx)
+    check_weights(w, rw, f"{name} T={T} E=64 k={k}")
+
+
 def test_route_unaligned_rows_take_scalar_path():
     base = _logits(301, 10, torch.bfloat16, seed=5)      # 20-byte rows: no 16-byte loads
     storage_t = torch.empty(301 * 10 + 3, dtype=torch.bfloat16, device=DEV)
