@@ -59,7 +59,7 @@ def test_route_matches_oracle(dt, T, E, k, renorm):
 
 @pytest.mark.parametrize("dt", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("k,renorm", [(8, True), (8, False), (3, True)])
-def test_route_e64_streamed_tiles(dt, k, renorm):
+def test_route_e64_many_waves(dt, k, renorm):
     """E = 64 at a size where 256-row tiles staged in shared memory run in several waves over
     the SMs (T = 2 x 3 x 152 x 256 + 77 rows), with a ragged last tile (ties, NaN, inf and -inf
     rows included)."""
