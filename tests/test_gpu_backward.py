@@ -195,6 +195,7 @@ def test_full_backward_chain_matches_oracle(dt):
     ([0, 300, 0, 0, 5, 64, 0, 1], 256, 128),        # tensor cores: idle experts between others
     ([0, 0, 0, 0], 128, 64),                          # no rows at all: every gradient is zero
     ([700, 0, 3, 0, 0, 600], 192, 256),               # CTA pairs for dA, g/u, dinput
+    ([0] * 1000 + [200, 0, 0, 64] + [0] * 20, 64, 64),  # E = 1024, 1022 idle experts
 ])
 def test_experts_backward_writes_every_gradient(counts, H, I):
     """Through the C ABI with dinput and the FP32 weight-gradient buffers filled with NaN: the
