@@ -9,8 +9,10 @@
  *
  * Conventions shared by every entry point
  *  - Buffers are DEVICE pointers owned by the caller, contiguous and row-major.  The library never
- *    allocates, frees or synchronises on these paths; scratch memory comes from the caller through
- *    (ws, ws_bytes), sized by the matching *_workspace_bytes() query.
+ *    allocates device memory, frees or synchronises on these paths; scratch memory comes from the
+ *    caller through (ws, ws_bytes), sized by the matching *_workspace_bytes() query.  (The one
+ *    other resource: moe_experts_backward keeps a second stream per device and creates two
+ *    events per call, see there.)
  *  - Work is enqueued on the caller's stream `stream` (a cudaStream_t; NULL = legacy default
  *    stream).  Every call returns as soon as the work is enqueued.
  *  - Every argument is checked on the host before anything is enqueued; a rejected call enqueues
